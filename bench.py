@@ -1,0 +1,461 @@
+"""Benchmark of the pi-Attention hot path on one GB300 (or N replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C4] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of synthetic input: the
+fused forward (band tiles + skip gather + GQA + epilogue) for the forward
+workloads, forward + backward for the training workload C5.  The default
+workload is C4 (B1 H16 Hkv4 N65536 d128 k256 pi1024 S4, bf16), the N=65536
+configuration the roofline target is stated for.
+
+Prints one JSON line.  `value` is tokens/s (B*N per step, summed over ranks);
+the line also carries useful TFLOP/s (4d FLOPs per attended pair forward, 8d
+backward), the roofline of the dominant kernel against the measured peaks in
+MEASURED_PEAKS.json, the fp64 oracle timed on this host's cores on a bounded
+sample (`cpu_baseline`), an end-to-end number through the public API with
+host buffers (`e2e`), the number of kernel launches, and the SM clocks sampled
+during the timed region.  `--impl reference` times the oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from structured_sparse_long_gb300.synth import MODE_ECP, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "sparse-attn tokens/s and useful TFLOP/s at N=4K–64K; % of roofline (1×GB300)"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def pairs_per_head(N, k, period, S, mode) -> int:
+    """Attended (query, key) pairs of one (b, h), closed forms of the neighbour sets."""
+    if mode == MODE_ECP:
+        c, total, s = k, 0, 0
+        while s * c < N:
+            n = min(c, N - s * c)
+            total += n * (n + 1) // 2 if s == 0 else n * (c + 1) + n * (n - 1) // 2
+            s += 1
+        return total
+    band = N * (k + 1) - k * (k + 1) // 2 if k < N else N * (N + 1) // 2
+    skip = sum(max(0, N - m * period) for m in range(1, S + 1) if m * period > k)
+    return band + skip
+
+
+def work(w, backward: bool):
+    esz = 4 if w.dtype == "f32" else 2
+    pairs = pairs_per_head(w.N, w.k_local, w.period, w.S, w.mode) * w.B * w.H
+    qo = w.B * w.H * w.N * w.d * esz
+    kv = w.B * w.Hkv * w.N * w.d * esz
+    vec = w.B * w.H * w.N * 4
+    fwd_bytes = 2 * qo + 2 * kv + vec * (2 if w.mode != MODE_ECP else 1)
+    fwd_flops = 4 * w.d * pairs
+    res = {"pairs": pairs, "fwd_bytes": fwd_bytes, "fwd_flops": fwd_flops,
+           "bytes": fwd_bytes, "flops": fwd_flops}
+    if backward:
+        bwd_bytes = 4 * qo + 4 * kv + 3 * vec
+        res.update(bwd_bytes=bwd_bytes, bwd_flops=8 * w.d * pairs, bwd_flops_10d=10 * w.d * pairs,
+                   bytes=fwd_bytes + bwd_bytes, flops=fwd_flops + 8 * w.d * pairs)
+    return res
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h"):
+        with open(os.path.join(ROOT, "structured_sparse_long_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the forward kernel from a committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"pi_fwd_tc_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        under_load = [x for x in sm if mx is None or x >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(under_load), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+class OracleSample:
+    """The fp64 oracle forward on this host's cores over the last `npos` positions of the
+    sequence (all batches and heads) -- a bounded sample of the workload."""
+
+    def __init__(self, w):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.inp = make_inputs(w, with_dout=False)
+        self.cores = oracle.threads()
+
+    def run(self, npos: int) -> float:
+        w = self.w
+        t0 = time.perf_counter()
+        self.oracle.fwd(self.inp["q"], self.inp["k"], self.inp["v"], self.inp["alpha"], w.k_local,
+                        w.period, w.S, w.mode, rows=(w.N - npos, w.N))
+        return time.perf_counter() - t0
+
+    def size_for(self, target_s: float) -> int:
+        cal = min(self.w.N, 64)
+        t_cal = self.run(cal)
+        return int(min(self.w.N, max(cal, cal * target_s / max(t_cal, 1e-6))))
+
+    def describe(self, npos: int) -> str:
+        w = self.w
+        text = (f"fp64 oracle forward over the last {npos} of {w.N} positions, all {w.B}x{w.H} "
+                f"(batch, head) rows; tokens/s = {w.B}*{npos}/t")
+        if w.backward:
+            text += " (forward only: the oracle backward has no row-range form)"
+        return text
+
+
+def cpu_baseline(w, target_s=10.0):
+    """Returns (tokens/s, cores, sample description) of the oracle on a bounded sample."""
+    smp = OracleSample(w)
+    npos = smp.size_for(target_s)
+    t = smp.run(npos)
+    return w.B * npos / t, smp.cores, smp.describe(npos)
+
+
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    """Max of a per-rank float over all ranks (the slowest rank times the job)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reference_arm(args, w, rank, world):
+    """The oracle as the reference implementation: rank 0 only, on host cores."""
+    if rank != 0:
+        return
+    smp = OracleSample(w)
+    npos = smp.size_for(min(8.0, 150.0 / (args.warmup + args.steps)))
+    for _ in range(args.warmup):
+        smp.run(npos)
+    per_step = [smp.run(npos) for _ in range(args.steps)]
+    value = w.B * npos * len(per_step) / sum(per_step)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(per_step) / len(per_step), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(w, "host cores, no GPU"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.cores,
+                             "kind": "oracle", "sample": smp.describe(npos)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def config_block(w, l2_note):
+    return {"workload": f"{w.name}: {w.description}", "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
+            "d": w.d, "k_local": w.k_local, "period": w.period, "S": w.S,
+            "mode": "ecp" if w.mode == MODE_ECP else "pi", "input_dtype": w.dtype, "l2": l2_note}
+
+
+def gpu_arm(args, w, rank, world, local_rank):
+    import structured_sparse_long_gb300 as pa
+    from structured_sparse_long_gb300 import build as pbuild
+
+    if rank == 0 or not os.path.exists(pbuild.LIB_PATH):
+        pbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pa.load()
+    stream = torch.cuda.current_stream(dev)
+
+    inp = make_inputs(w, with_dout=w.backward)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    bufs = {}
+    if w.backward:
+        bufs = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]),
+                    dv=torch.empty_like(d["v"]),
+                    dalpha=torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32),
+                    ws=torch.empty(max(16, pa.bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)),
+                                   device=dev, dtype=torch.uint8))
+
+    def fwd():
+        pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
+               lse=lse, stream=stream)
+
+    def bwd():
+        pa.bwd(d["q"], d["k"], d["v"], d["alpha"], out, lse, d["dout"], w.k_local, w.period, w.S,
+               w.mode, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], dalpha=bufs["dalpha"],
+               workspace=bufs["ws"], stream=stream)
+
+    # (name, launcher, kernels it launches)
+    phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 3)] if w.backward else [])
+    wk = work(w, w.backward)
+    flush = wk["bytes"] < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, device=dev, dtype=torch.float32) if flush else None
+    l2_note = ("L2 flushed between steps (write of a 2x L2 buffer outside the timed events)"
+               if flush else f"inputs larger than L2 ({wk['bytes'] / 1e6:.0f} MB moved per step)")
+
+    def step(record=None):
+        for name, fn, _ in phases:
+            if record is not None:
+                record[name][0].record(stream)
+            fn()
+            if record is not None:
+                record[name][1].record(stream)
+
+    for _ in range(args.warmup):
+        if flush:
+            scratch.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if pa.status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for n, _, _ in phases} for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        if flush:
+            scratch.zero_()
+        step(ev[k])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    status = pa.status()
+    if status != 0:
+        raise RuntimeError(f"device status word {status} after the timed region")
+
+    per_phase = {n: [e[n][0].elapsed_time(e[n][1]) for e in ev] for n, _, _ in phases}
+    step_ms = [sum(per_phase[n][k] for n, _, _ in phases) for k in range(args.steps)]
+    total_ms = sum(step_ms)
+    total_ms = reduce_max(total_ms, world, dev if args.backend == "nccl" else "cpu")
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = w.B * w.N * world
+    value = tokens_per_step * args.steps / (total_ms / 1e3)
+    tflops = wk["flops"] * world * args.steps / (total_ms / 1e3) / 1e12
+
+    # dominant kernel roofline (forward kernel: the whole step for the forward workloads)
+    peaks, peak_kind = load_peaks()
+    dom = max(per_phase, key=lambda n: sum(per_phase[n]))
+    dom_ms = statistics.mean(per_phase[dom])
+    dom_bytes = wk["fwd_bytes"] if dom == "pi_attn_fwd" else wk["bwd_bytes"]
+    dom_flops = wk["fwd_flops"] if dom == "pi_attn_fwd" else wk["bwd_flops"]
+    hbm = peaks["hbm_gbs"]
+    tensor = peaks["bf16_tflops"]
+    t_hbm = dom_bytes / (hbm * 1e9)
+    t_tensor = dom_flops / (tensor * 1e12)
+    bound = "hbm" if t_hbm >= t_tensor else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = dom_bytes / (dom_ms / 1e3) / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = dom_flops / (dom_ms / 1e3) / 1e12, tensor, "TFLOP/s"
+    traffic = profiled_traffic(w.name) if dom == "pi_attn_fwd" else None
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}, burst)",
+                "t_roof_us": 1e6 * max(t_hbm, t_tensor), "t_hbm_us": 1e6 * t_hbm,
+                "t_tensor_us": 1e6 * t_tensor, "kernel_us": 1e3 * dom_ms,
+                "algorithmic_bytes": dom_bytes, "useful_flops": dom_flops,
+                "tensor_frac_of_peak": dom_flops / (dom_ms / 1e3) / 1e12 / tensor}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {n: (t.pin_memory() if t is not None else None) for n, t in inp.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for n, t in host.items()
+                  if t is not None and (n != "dout" or w.backward))
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        grads_h = {}
+        if w.backward:
+            grads_h = {n: torch.empty(bufs[n].shape, dtype=bufs[n].dtype).pin_memory()
+                       for n in ("dq", "dk", "dv", "dalpha")}
+            d2h += sum(t.numel() * t.element_size() for t in grads_h.values())
+
+        def e2e_step():
+            for n, t in host.items():
+                if t is not None and (n != "dout" or w.backward):
+                    d[n].copy_(t, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            for n, t in grads_h.items():
+                t.copy_(bufs[n], non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        e_ms = reduce_max(e_ms, world, dev if args.backend == "nccl" else "cpu")
+        e2e = {"value": tokens_per_step * n_e2e / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / n_e2e, "steps": n_e2e}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tps, cores, desc = cpu_baseline(w, target_s=args.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded torch.Generator, shapes of the workload)",
+            "config": config_block(w, l2_note), "useful_tflops": tflops,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * sum(n for _, _, n in phases),
+            "clocks": clocks, "per_phase_ms": {n: statistics.mean(v) for n, v in per_phase.items()},
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="C4", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.config]
+    if args.impl == "reference":
+        reference_arm(args, w, rank, world)
+        return
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(args.backend)
+    try:
+        gpu_arm(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

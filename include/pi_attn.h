@@ -1,0 +1,191 @@
+/*
+ * pi_attn.h -- C ABI of the GB300 (sm_103a) pi-Attention / ECP attention library.
+ *
+ * Operation.  For every batch b, query head h and query position i, one
+ * softmax runs over the union U(i) of two key sets, and the output is the
+ * softmax-weighted sum of the value rows:
+ *
+ *   pi mode ("pi-Attention: Periodic Sparse Transformers for Efficient
+ *   Long-Context Modeling", section 2 "Methodology"):
+ *     L(i) = { j : max(0, i - k_local) <= j <= i }          (2.1 ring-local band,
+ *                                                           causal, both ends kept)
+ *     P(i) = { i - m*period : m = 1..S, i - m*period >= 0,
+ *              m*period > k_local }                        (2.2 pi-skip keys,
+ *                                                           causal; a skip key
+ *                                                           already in the band is
+ *                                                           not repeated)
+ *     z_ij = (q_i . k_j) / sqrt(d) + ln(alpha_i)     for j in L(i)
+ *     z_ij = (q_i . k_j) / sqrt(d) + ln(1 - alpha_i) for j in P(i)   (2.3 gate as
+ *                                                           log-prior, one softmax
+ *                                                           over the union)
+ *   ECP mode ("Efficient Context Propagating Perceiver Architectures for
+ *   Auto-Regressive Language Modeling", section 2, paired-segment PAR block):
+ *     with half-segment length c = k_local and s = floor(i / c):
+ *     U(i) = { j : max(0, (s - 1) * c) <= j <= i },  z_ij = (q_i . k_j) / sqrt(d)
+ *   GQA (attention branch of the GSS-Transformer hybrid page): query head h
+ *   reads key/value head floor(h / (H / Hkv)).
+ *
+ *   lse_i = ln sum_{j in U(i)} exp(z_ij);  out_i = sum_j exp(z_ij - lse_i) v_j.
+ *   A row with no finite logit (alpha_i = 0 and P(i) empty) gets out_i = 0 and
+ *   lse_i = -inf.
+ *
+ * Layouts (all contiguous, row-major, element strides implied by the shape):
+ *   q, out, dq, dout : [B, H,   N, d]
+ *   k, v, dk, dv     : [B, Hkv, N, d]
+ *   alpha, lse, dalpha : [B, H, N] fp32
+ * "bf16" entry points take bfloat16 q/k/v/out/dout/dq/dk/dv; "_f32" entry
+ * points take fp32.  alpha, lse and dalpha are always fp32.
+ *
+ * Ownership.  The caller owns every buffer and the stream.  The library never
+ * allocates per call; the only device state it keeps is one int status word
+ * per device, a static device variable.
+ *
+ * Asynchrony.  Every compute entry point only enqueues work on `stream`
+ * (a cudaStream_t passed as void*, NULL = legacy default stream) and returns
+ * PI_OK once the kernels are launched.  Device-side failures (a bounded wait
+ * that ran out) are reported later by pi_attn_status().
+ *
+ * Validation.  Every argument is checked before anything is launched; a bad
+ * argument returns a negative pi_status_t and launches nothing:
+ *   PI_ERR_NULL        a required pointer is NULL (alpha may be NULL only in
+ *                      ECP mode, where it is unused)
+ *   PI_ERR_SHAPE       B, H, Hkv, N <= 0; H % Hkv != 0; k_local < 0; S < 0;
+ *                      period <= 0 while S > 0; ECP with k_local <= 0 or S != 0
+ *   PI_ERR_UNSUPPORTED d not in {32, 64, 128}; unknown mode; sizes whose
+ *                      element offsets overflow int64 or whose row count
+ *                      exceeds 2^31-1; (debug calls) N above their limit
+ *   PI_ERR_ALIGN       a bf16/fp32 tensor of shape [.., d] not 16-byte aligned,
+ *                      or an fp32 vector (alpha, lse, dalpha) not 4-byte aligned
+ *   PI_ERR_WORKSPACE   backward workspace NULL or smaller than required
+ *   PI_ERR_CUDA        a CUDA runtime error at launch (cudaGetLastError)
+ *   PI_ERR_DEVICE_TIMEOUT  (from pi_attn_status) a device-side bounded wait
+ *                      gave up; the kernel returned without finishing.  The
+ *                      status word is sticky: until pi_attn_status() reads and
+ *                      clears it, later launches on that device give up at their
+ *                      first wait that is not already satisfied, so their
+ *                      outputs are undefined.
+ */
+#ifndef PI_ATTN_H_
+#define PI_ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PI_MODE_PI = 0, PI_MODE_ECP = 1 } pi_mode_t;
+
+typedef enum {
+    PI_OK = 0,
+    PI_ERR_NULL = -1,
+    PI_ERR_SHAPE = -2,
+    PI_ERR_UNSUPPORTED = -3,
+    PI_ERR_ALIGN = -4,
+    PI_ERR_WORKSPACE = -5,
+    PI_ERR_CUDA = -6,
+    PI_ERR_DEVICE_TIMEOUT = -7
+} pi_status_t;
+
+/*
+ * pi_attn_fwd -- fused sparse causal attention forward, bf16 in/out, fp32
+ * accumulation (pi-Attention section 2.1-2.3; ECP section 2).
+ *   q [B,H,N,d], k/v [B,Hkv,N,d] bf16 (device); alpha [B,H,N] fp32 (device,
+ *   values in [0,1]; may be NULL in ECP mode); k_local = band width k (pi
+ *   mode) or half-segment length c (ECP mode); period = skip stride pi;
+ *   S = number of skip multiples (0 = band only); mode = pi_mode_t.
+ *   Writes out [B,H,N,d] bf16 (round-to-nearest-even) and lse [B,H,N] fp32
+ *   (natural log).  d = 64 and 128 run on the tcgen05/TMEM/TMA kernel; d = 32
+ *   runs on the CUDA-core kernel.  Deterministic.
+ */
+int pi_attn_fwd(const void *q, const void *k, const void *v, const float *alpha,
+                int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
+                void *out, float *lse, void *stream);
+
+/* pi_attn_fwd_f32 -- same operation and arguments with fp32 q/k/v/out (CUDA-core
+ * kernel, fp32 throughout).  Deterministic. */
+int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *alpha,
+                    int B, int H, int Hkv, int N, int d, int k_local, int period, int S,
+                    int mode, void *out, float *lse, void *stream);
+
+/*
+ * pi_attn_bwd_workspace_size -- bytes of device workspace pi_attn_bwd needs
+ * for these sizes (one fp32 per query row for D_i = dout_i . out_i).
+ */
+size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * pi_attn_bwd -- backward of pi_attn_fwd (the chain rule through the
+ * definition above; bf16 tensors, fp32 accumulation).
+ *   Inputs: q, k, v, alpha as for the forward; out [B,H,N,d] and lse [B,H,N]
+ *   from pi_attn_fwd; dout [B,H,N,d].
+ *   Outputs: dq [B,H,N,d], dk and dv [B,Hkv,N,d] (summed over the query heads
+ *   of each KV group) bf16; dalpha [B,H,N] fp32 (may be NULL; zero in ECP mode),
+ *   computed as dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)),
+ *   which equals sum_L dz/alpha - sum_P dz/(1-alpha) because every softmax row
+ *   of dz sums to zero; it is undefined for alpha_i in {0, 1} when P(i) is not
+ *   empty.  dz_ij = p_ij (dout_i . v_j - dout_i . out_i).
+ *   workspace: device buffer of at least pi_attn_bwd_workspace_size() bytes,
+ *   owned by the caller, contents ignored on entry.  Deterministic.
+ */
+int pi_attn_bwd(const void *q, const void *k, const void *v, const float *alpha,
+                const void *out, const float *lse, const void *dout,
+                int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
+                void *dq, void *dk, void *dv, float *dalpha,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* pi_attn_bwd_f32 -- same with fp32 tensors. */
+int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *alpha,
+                    const void *out, const float *lse, const void *dout,
+                    int B, int H, int Hkv, int N, int d, int k_local, int period, int S,
+                    int mode, void *dq, void *dk, void *dv, float *dalpha,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pi_attn_status -- synchronises `stream`, reads the current device's status
+ * word, resets it to PI_OK and returns what it held (PI_OK or
+ * PI_ERR_DEVICE_TIMEOUT), or PI_ERR_CUDA if the synchronisation failed.
+ */
+int pi_attn_status(void *stream);
+
+/* pi_attn_strerror -- static, human-readable name of a pi_status_t. */
+const char *pi_attn_strerror(int code);
+
+/*
+ * pi_attn_debug_counts -- runs the forward (dtype 0 = bf16 kernel chosen as in
+ * pi_attn_fwd, 1 = fp32 kernel) and, from that kernel's own tile walk and
+ * masks, also writes count [B,H,N] int32 = number of keys the row attended
+ * and idx_sum [B,H,N] int64 = sum of their key positions.  Used to check the
+ * neighbour enumeration bit-exactly.  Arguments otherwise as pi_attn_fwd.
+ */
+int pi_attn_debug_counts(const void *q, const void *k, const void *v, const float *alpha,
+                         int B, int H, int Hkv, int N, int d, int k_local, int period, int S,
+                         int mode, int dtype, void *out, float *lse, int *count,
+                         long long *idx_sum, void *stream);
+
+/*
+ * pi_attn_debug_probs -- for N <= 2048: runs the forward (writing out and lse
+ * as pi_attn_fwd does) and, from the same kernel's tile walk and masks, writes
+ * the normalised probability exp(z_ij - lse_in_i) into P [B,H,N,N] fp32 for
+ * every key j the row attends to; lse_in must be the lse of an earlier forward
+ * on the same inputs.  Entries for keys the row does not attend to are not
+ * written: the caller zero-fills P.  dtype as in pi_attn_debug_counts.
+ */
+int pi_attn_debug_probs(const void *q, const void *k, const void *v, const float *alpha,
+                        const float *lse_in, int B, int H, int Hkv, int N, int d, int k_local,
+                        int period, int S, int mode, int dtype, void *out, float *lse, float *P,
+                        void *stream);
+
+/*
+ * pi_attn_debug_wait_timeout -- launches one block that waits on a shared-memory
+ * barrier nothing ever completes, giving up after timeout_us microseconds;
+ * it then records PI_ERR_DEVICE_TIMEOUT in the status word and returns.
+ * Exercises the bounded-wait error path without faulting the GPU.
+ */
+int pi_attn_debug_wait_timeout(int timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PI_ATTN_H_ */

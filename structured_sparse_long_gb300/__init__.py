@@ -1,0 +1,15 @@
+"""GB300 (sm_103a) pi-Attention / ECP fused sparse causal attention.
+
+The product is the C-ABI library ``libpi_attn.so`` (include/pi_attn.h) built
+from ``csrc/`` for sm_103a.  This package holds that source, the nvcc build
+script, a thin ctypes binding with the same names as the C entry points, and
+the seeded synthetic input generators.  Importing the package loads nothing;
+the first call loads the library and fails loudly if it is missing.
+"""
+from ._binding import (MODE_ECP, MODE_PI, PiAttnError, bwd, bwd_workspace_size,  # noqa: F401
+                       debug_counts, debug_probs, debug_wait_timeout, fwd, lib_path, load,
+                       status, strerror)
+
+__all__ = ["fwd", "bwd", "bwd_workspace_size", "status", "strerror", "debug_counts",
+           "debug_probs", "debug_wait_timeout", "load", "lib_path", "PiAttnError",
+           "MODE_PI", "MODE_ECP"]

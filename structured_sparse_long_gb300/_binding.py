@@ -1,0 +1,207 @@
+"""ctypes binding of libpi_attn.so: argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks that their dtype, layout
+and device match what the C ABI expects, and passes raw device pointers, sizes
+and the current CUDA stream to the entry point of the same name in
+include/pi_attn.h.  All computation runs in the library's CUDA kernels; there
+is no fallback: if the library is not built or cannot be loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MODE_PI = 0
+MODE_ECP = 1
+PI_OK = 0
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PiAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpi_attn.so (built by structured_sparse_long_gb300.build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing; "
+                               "run structured_sparse_long_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        fwd_args = [P, P, P, P] + [I] * 9 + [P, P, P]
+        lib.pi_attn_fwd.argtypes = fwd_args
+        lib.pi_attn_fwd_f32.argtypes = fwd_args
+        bwd_args = [P, P, P, P, P, P, P] + [I] * 9 + [P, P, P, P, P, Z, P]
+        lib.pi_attn_bwd.argtypes = bwd_args
+        lib.pi_attn_bwd_f32.argtypes = bwd_args
+        lib.pi_attn_bwd_workspace_size.argtypes = [I] * 5
+        lib.pi_attn_bwd_workspace_size.restype = Z
+        lib.pi_attn_status.argtypes = [P]
+        lib.pi_attn_strerror.argtypes = [I]
+        lib.pi_attn_strerror.restype = ctypes.c_char_p
+        lib.pi_attn_debug_counts.argtypes = [P, P, P, P] + [I] * 10 + [P, P, P, P, P]
+        lib.pi_attn_debug_probs.argtypes = [P, P, P, P, P] + [I] * 10 + [P, P, P, P]
+        lib.pi_attn_debug_wait_timeout.argtypes = [I, P]
+        for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
+                     "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
+                     "pi_attn_debug_wait_timeout"):
+            getattr(lib, name).restype = I
+        _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    return load().pi_attn_strerror(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != PI_OK:
+        raise PiAttnError(fn, code, strerror(code))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _expect(t: torch.Tensor, name: str, dtype, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _sizes(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B,H,N,d] and k [B,Hkv,N,d]")
+    B, H, N, d = q.shape
+    return B, H, k.shape[1], N, d
+
+
+def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
+        out=None, lse=None, stream=None):
+    """pi_attn_fwd (bf16) / pi_attn_fwd_f32 (fp32), chosen by q.dtype. Returns (out, lse)."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _expect(t, n, dt)
+    _expect(v, "v", dt, k.shape)
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H, N))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _expect(out, "out", dt, q.shape)
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    lib = load()
+    fn = {torch.bfloat16: lib.pi_attn_fwd, torch.float32: lib.pi_attn_fwd_f32}.get(dt)
+    if fn is None:
+        raise ValueError(f"unsupported dtype {dt}")
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d, k_local, period, S, mode,
+            _ptr(out), _ptr(lse), _stream(stream))
+    _check(fn.__name__, rc)
+    return out, lse
+
+
+def bwd_workspace_size(B, H, Hkv, N, d) -> int:
+    return int(load().pi_attn_bwd_workspace_size(B, H, Hkv, N, d))
+
+
+def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode: int = MODE_PI,
+        dq=None, dk=None, dv=None, dalpha=None, workspace=None, stream=None):
+    """pi_attn_bwd (bf16) / pi_attn_bwd_f32, chosen by q.dtype. Returns (dq, dk, dv, dalpha)."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    dt = q.dtype
+    for t, n in ((q, "q"), (out, "out"), (dout, "dout")):
+        _expect(t, n, dt, q.shape)
+    for t, n in ((k, "k"), (v, "v")):
+        _expect(t, n, dt, k.shape)
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H, N))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dalpha is None:
+        dalpha = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    nbytes = bwd_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+    lib = load()
+    fn = {torch.bfloat16: lib.pi_attn_bwd, torch.float32: lib.pi_attn_bwd_f32}.get(dt)
+    if fn is None:
+        raise ValueError(f"unsupported dtype {dt}")
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse), _ptr(dout),
+            B, H, Hkv, N, d, k_local, period, S, mode, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(fn.__name__, rc)
+    return dq, dk, dv, dalpha
+
+
+def status(stream=None) -> int:
+    """pi_attn_status: synchronise and return (and clear) the device status word."""
+    return int(load().pi_attn_status(_stream(stream)))
+
+
+def debug_counts(q, k, v, alpha, k_local, period, S, mode=MODE_PI, stream=None):
+    """pi_attn_debug_counts. Returns (out, lse, count int32 [B,H,N], idx_sum int64 [B,H,N])."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    cnt = torch.empty((B, H, N), device=q.device, dtype=torch.int32)
+    isum = torch.empty((B, H, N), device=q.device, dtype=torch.int64)
+    dtype = 1 if q.dtype == torch.float32 else 0
+    rc = load().pi_attn_debug_counts(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d,
+                                     k_local, period, S, mode, dtype, _ptr(out), _ptr(lse),
+                                     _ptr(cnt), _ptr(isum), _stream(stream))
+    _check("pi_attn_debug_counts", rc)
+    return out, lse, cnt, isum
+
+
+def debug_probs(q, k, v, alpha, lse_in, k_local, period, S, mode=MODE_PI, stream=None):
+    """pi_attn_debug_probs. Returns the dense probabilities P [B,H,N,N] fp32."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    P = torch.zeros((B, H, N, N), device=q.device, dtype=torch.float32)
+    dtype = 1 if q.dtype == torch.float32 else 0
+    rc = load().pi_attn_debug_probs(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(lse_in), B, H,
+                                    Hkv, N, d, k_local, period, S, mode, dtype, _ptr(out),
+                                    _ptr(lse), _ptr(P), _stream(stream))
+    _check("pi_attn_debug_probs", rc)
+    return P
+
+
+def debug_wait_timeout(timeout_us: int, stream=None) -> None:
+    rc = load().pi_attn_debug_wait_timeout(int(timeout_us), _stream(stream))
+    _check("pi_attn_debug_wait_timeout", rc)

@@ -1,0 +1,800 @@
+// pi_fwd_tc.cu -- fused pi-Attention / ECP forward on sm_103a tensor cores.
+//
+// What it computes ("pi-Attention: Periodic Sparse Transformers for Efficient
+// Long-Context Modeling", section 2.1-2.3; ECP page section 2; GQA from the
+// GSS-Transformer hybrid page): for each query row i, one softmax over the
+// causal band [lo(i), i] and the skip keys i - m*period (pi mode), with
+// log2(alpha) added to band logits and log2(1 - alpha) to skip logits, and the
+// softmax-weighted sum of value rows.
+//
+// How (one CTA = 128 query rows = the M of every MMA):
+//   * GQA packing: the 128 rows are GP query heads of one KV group x R = 128/GP
+//     consecutive positions, so every K/V tile staged in shared memory serves
+//     all GP heads at once.
+//   * Keys are walked in 32-key chunks (one TMA box each).  A chunk is either a
+//     band chunk (keys lo(p0) + 32c ...) or a skip chunk: the keys i - m*period
+//     of the block's rows form R consecutive keys, so one skip block is R/32
+//     chunks; each row attends to exactly one column of it (the "diagonal").
+//     Two chunks make one key tile (N <= 64).
+//   * Warp 0 (lane 0) streams Q and K tiles with TMA, warp 2 (lane 0) streams V
+//     tiles; warp 1 (lane 0) issues tcgen05.mma: S = Q K^T into one of two
+//     64-column TMEM buffers, then O += P V with P read from TMEM.
+//   * Warps 4-7 run the softmax, one thread per row (TMEM lane = row): masks,
+//     adds the prior, keeps the running max m and sum l (rescaling O in TMEM
+//     only when the max grows by more than 2^8), writes P as bf16 over its S,
+//     and finally normalises O, stages it in shared memory and TMA-stores it.
+//   * Every wait is bounded; a wait that runs out sets the device status word
+//     and the CTA unwinds without hanging.
+#include <cuda.h>
+
+#include "pi_common.cuh"
+#include "pi_launch.h"
+
+namespace pi {
+namespace tc {
+
+constexpr int BM = 128;           // rows per CTA (MMA M)
+constexpr int CHUNK = 32;         // keys per chunk (TMA box rows)
+constexpr int TILE_N = 64;        // keys per tile (2 chunks)
+constexpr int NUM_THREADS = 256;
+constexpr int TMEM_COLS = 256;    // S buffers [0,128), O [128, 128+d)
+constexpr int O_COL = 128;
+constexpr int ROW_BYTES = 128;    // one 64-element bf16 swizzle row
+constexpr int BOX_BYTES = CHUNK * ROW_BYTES;  // one 64 x 32 TMA box
+constexpr float kRescaleThreshold = 8.f;      // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int KD = D / 64;  // 64-element column blocks of d
+    static constexpr int STAGES = (D == 64) ? 4 : 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_STAGE = TILE_N * D * 2;
+    static constexpr int KV_DBLK = TILE_N * ROW_BYTES;  // one 64-column block of a stage
+    static constexpr int Q_DBLK = BM * ROW_BYTES;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + Q_BYTES;
+    static constexpr int V_OFF = K_OFF + STAGES * KV_STAGE;
+    static constexpr int BAR_OFF = V_OFF + STAGES * KV_STAGE;
+    // barrier indices
+    static constexpr int B_Q = 0;
+    static constexpr int B_KF = 1;
+    static constexpr int B_KE = B_KF + STAGES;
+    static constexpr int B_VF = B_KE + STAGES;
+    static constexpr int B_VE = B_VF + STAGES;
+    static constexpr int B_SF = B_VE + STAGES;
+    static constexpr int B_PR = B_SF + 2;
+    static constexpr int B_PV = B_PR + 2;
+    static constexpr int B_DR = B_PV + 1;
+    static constexpr int NBARS = B_DR + 1;
+    static constexpr int MISC_BYTES = NBARS * 8 + 16;
+    static constexpr int SMEM_BYTES = BAR_OFF + MISC_BYTES + 1024;  // + alignment slack
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+struct WaitCtx {
+    volatile uint32_t *abort;
+    int *status;
+    uint64_t timeout_ns;
+};
+
+// Bounded wait on the phase of `bar` with the given parity.  Gives up when the
+// CTA's abort flag is raised, when another CTA has already recorded a failure in
+// the device status word (so a failing launch drains in one wave), or after
+// timeout_ns (then raises the flag and records the timeout).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx &w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (w.status && *reinterpret_cast<volatile int *>(w.status) != kStatusOk) {
+            *w.abort = 1u;
+            return false;
+        }
+        if (global_ns() - t0 > w.timeout_ns) {
+            *w.abort = 1u;
+            record_status(w.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+#define PI_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                 "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : PI_R8(0), PI_R8(8), PI_R8(16), PI_R8(24)
+        : "r"(taddr));
+}
+#undef PI_R8
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
+    tmem_st16(taddr, v);
+    tmem_st16(taddr + 16, v + 16);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
+// offsets, descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, M x N, operand majors.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct TcArgs {
+    const float *alpha;
+    float *lse;
+    Shape s;
+    int GP;  // query heads packed per CTA
+    int *status;
+    uint64_t timeout_ns;
+    int *cnt;
+    long long *isum;
+    const float *lse_in;
+    float *P;
+};
+
+// Key chunk ci of the block: first key position, whether it is a skip chunk,
+// its skip distance m*period and sub-block index u.
+struct ChunkWalk {
+    int lo0, n_band, m_first, cpb, p0, period;
+    __device__ __forceinline__ int key0(int ci, int &back, int &u, bool &skip) const {
+        if (ci < n_band) {
+            back = 0; u = 0; skip = false;
+            return lo0 + ci * CHUNK;
+        }
+        const int sc = ci - n_band;
+        const int m = m_first + sc / cpb;
+        u = sc % cpb;
+        back = m * period;
+        skip = true;
+        return p0 - back + u * CHUNK;
+    }
+};
+
+template <int D, int DBG>
+__global__ void __launch_bounds__(NUM_THREADS, 2)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const TcArgs args) {
+    using C = Cfg<D>;
+    constexpr int ST = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const uint32_t sQ = sbase + C::Q_OFF, sK = sbase + C::K_OFF, sV = sbase + C::V_OFF;
+    const uint32_t sBar = sbase + C::BAR_OFF;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NBARS * 8);
+    uint32_t *tmem_slot = misc;
+    volatile uint32_t *abort_flag = misc + 1;
+    auto bar = [&](int idx) -> uint32_t { return sBar + idx * 8; };
+
+    const Shape &s = args.s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtx wc{abort_flag, args.status, args.timeout_ns};
+
+    // ---- block coordinates: (b, head group, position block), positions fastest
+    const int GP = args.GP;
+    const int R = BM / GP;
+    const int nqb = (s.N + R - 1) / R;
+    const int hsub = s.H / GP;
+    int bid = blockIdx.x;
+    const int pb = bid % nqb;
+    bid /= nqb;
+    const int hs = bid % hsub;
+    const int b = bid / hsub;
+    const int h0 = hs * GP;
+    const int g = h0 / (s.H / s.Hkv);
+    const int p0 = pb * R;
+
+    // ---- key chunks of this block
+    ChunkWalk cw;
+    cw.p0 = p0;
+    cw.period = s.period;
+    cw.cpb = R / CHUNK;
+    cw.lo0 = band_lo(p0, s.mode, s.k_local);
+    const int band_hi = min(s.N - 1, p0 + R - 1);
+    cw.n_band = (band_hi - cw.lo0) / CHUNK + 1;
+    int n_skip_blocks = 0;
+    cw.m_first = 1;
+    if (s.mode == 0 && s.S > 0) {
+        cw.m_first = max(1, s.k_local / s.period + 1);  // smallest m with m*period > k
+        const int m_last = min(s.S, (p0 + R - 1) / s.period);
+        n_skip_blocks = max(0, m_last - cw.m_first + 1);
+    }
+    const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
+    const int n_tiles = (n_chunks + 1) / 2;
+
+    // ---- setup: barriers, TMEM
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_Q), 1);
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(bar(C::B_KF + i), 1);
+            mbar_init(bar(C::B_KE + i), 1);
+            mbar_init(bar(C::B_VF + i), 1);
+            mbar_init(bar(C::B_VE + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_SF + i), 1);
+            mbar_init(bar(C::B_PR + i), 128);
+        }
+        mbar_init(bar(C::B_PV), 1);
+        mbar_init(bar(C::B_DR), 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= producer: Q and K tiles
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
+            for (int dc = 0; dc < C::KD; ++dc)
+                tma_load_3d(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q));
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % ST, round = t / ST;
+                if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
+                const int nch = min(2, n_chunks - 2 * t);
+                mbar_expect_tx(bar(C::B_KF + st), nch * C::KD * BOX_BYTES);
+                for (int cc = 0; cc < nch; ++cc) {
+                    int back, u;
+                    bool sk;
+                    const int key0 = cw.key0(2 * t + cc, back, u, sk);
+                    for (int dc = 0; dc < C::KD; ++dc)
+                        tma_load_3d(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
+                                    dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st));
+                }
+                issued = t + 1;
+            }
+            if (*abort_flag) {  // let loads in flight land before the CTA leaves
+                volatile uint32_t zero = 0;
+                WaitCtx w2{&zero, nullptr, 20000000ull};
+                wait_bar(bar(C::B_Q), 0, w2);
+                for (int t = max(0, issued - ST); t < issued; ++t)
+                    wait_bar(bar(C::B_KF + t % ST), (t / ST) & 1, w2);
+            }
+        }
+    } else if (warp == 2) {
+        // ================= producer: V tiles
+        if (lane == 0) {
+            prefetch_tmap(&tmV);
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % ST, round = t / ST;
+                if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
+                const int nch = min(2, n_chunks - 2 * t);
+                mbar_expect_tx(bar(C::B_VF + st), nch * C::KD * BOX_BYTES);
+                for (int cc = 0; cc < nch; ++cc) {
+                    int back, u;
+                    bool sk;
+                    const int key0 = cw.key0(2 * t + cc, back, u, sk);
+                    for (int dc = 0; dc < C::KD; ++dc)
+                        tma_load_3d(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
+                                    dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st));
+                }
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                volatile uint32_t zero = 0;
+                WaitCtx w2{&zero, nullptr, 20000000ull};
+                for (int t = max(0, issued - ST); t < issued; ++t)
+                    wait_bar(bar(C::B_VF + t % ST), (t / ST) & 1, w2);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0) {
+            bool ok = wait_bar(bar(C::B_Q), 0, wc);
+            for (int t = 0; ok && t <= n_tiles; ++t) {
+                if (t < n_tiles) {
+                    const int st = t % ST, buf = t & 1;
+                    if (!wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc)) break;
+                    if (t >= 2 && !wait_bar(bar(C::B_PV), (t - 2) & 1, wc)) break;
+                    tc_fence_after();
+                    const int nch = min(2, n_chunks - 2 * t);
+                    const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
+                    const uint32_t dS = tbase + buf * TILE_N;
+#pragma unroll
+                    for (int dc = 0; dc < C::KD; ++dc) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t a = sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024);
+                            const uint64_t bb =
+                                sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024);
+                            mma_ss(dS, a, bb, idesc, (dc | ks) != 0);
+                        }
+                    }
+                    tc_commit(bar(C::B_SF + buf));
+                    tc_commit(bar(C::B_KE + st));
+                }
+                if (t >= 1) {
+                    const int u = t - 1, st = u % ST, buf = u & 1;
+                    if (!wait_bar(bar(C::B_PR + buf), (u >> 1) & 1, wc)) break;
+                    if (!wait_bar(bar(C::B_VF + st), (u / ST) & 1, wc)) break;
+                    tc_fence_after();
+                    const int nch = min(2, n_chunks - 2 * u);
+                    const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
+                    const uint32_t aP = tbase + buf * TILE_N;
+                    for (int kk = 0; kk < 2 * nch; ++kk) {
+                        const uint64_t bb = sdesc(sV + st * C::KV_STAGE + kk * 16 * ROW_BYTES,
+                                                  C::KV_DBLK, 1024);
+                        mma_ts(tbase + O_COL, aP + kk * 8, bb, idesc, (u > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar(C::B_PV));
+                    tc_commit(bar(C::B_VE + st));
+                }
+            }
+            // every MMA issued so far has finished before TMEM is released
+            tc_commit(bar(C::B_DR));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp >= 4) {
+        // ================= softmax + epilogue: one thread per row
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const int hh = r / R, trow = r % R;
+        const int i = p0 + trow;
+        const int h = h0 + hh;
+        const bool row_ok = i < s.N;
+        const long long row_g = ((long long)b * s.H + h) * s.N + i;
+        const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
+        const float off_band = (s.mode == 0) ? log2f(al) : 0.f;
+        const float off_skip = log2f(1.f - al);
+        const int lo_i = band_lo(i, s.mode, s.k_local);
+        const float sc = s.scale_log2;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        float lse2_in = 0.f;
+        if (DBG == 2) lse2_in = row_ok ? args.lse_in[row_g] * kLog2e : -INFINITY;
+
+        float m_ref = -INFINITY, l = 0.f;
+        long long cnt = 0, isum = 0;
+        bool ok = true;
+
+        // valid column range [clo, chi] of chunk ci for this row, and its prior
+        auto chunk_range = [&](int ci, int &key0, int &clo, int &chi, float &off) {
+            int back, u;
+            bool sk;
+            key0 = cw.key0(ci, back, u, sk);
+            if (!sk) {
+                clo = max(lo_i - key0, 0);
+                chi = min(i - key0, CHUNK - 1);
+                off = off_band;
+            } else {
+                const int jk = i - back;
+                const int c = jk - key0;
+                if (jk >= 0 && c >= 0 && c < CHUNK) { clo = c; chi = c; }
+                else { clo = CHUNK; chi = -1; }
+                off = off_skip;
+            }
+        };
+
+        for (int t = 0; t < n_tiles; ++t) {
+            const int buf = t & 1;
+            ok = wait_bar(bar(C::B_SF + buf), (t >> 1) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            const int nch = min(2, n_chunks - 2 * t);
+            const uint32_t tS = tbase + lane_base + buf * TILE_N;
+            uint32_t ra[CHUNK], rb[CHUNK];
+            tmem_ld32(tS, ra);
+            if (nch > 1) tmem_ld32(tS + CHUNK, rb);
+            tmem_wait_ld();
+
+            int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
+            float offa, offb = 0.f;
+            chunk_range(2 * t, key0a, cloa, chia, offa);
+            if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb);
+
+            float *fa = reinterpret_cast<float *>(ra);
+            float *fb = reinterpret_cast<float *>(rb);
+            float mxa = -INFINITY, mxb = -INFINITY;
+            if (__all_sync(0xffffffffu, cloa <= 0 && chia >= CHUNK - 1)) {
+#pragma unroll
+                for (int c = 0; c < CHUNK; ++c) mxa = fmaxf(mxa, fa[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < CHUNK; ++c) {
+                    fa[c] = (c >= cloa && c <= chia) ? fa[c] : -INFINITY;
+                    mxa = fmaxf(mxa, fa[c]);
+                }
+            }
+            if (nch > 1) {
+                if (__all_sync(0xffffffffu, clob <= 0 && chib >= CHUNK - 1)) {
+#pragma unroll
+                    for (int c = 0; c < CHUNK; ++c) mxb = fmaxf(mxb, fb[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < CHUNK; ++c) {
+                        fb[c] = (c >= clob && c <= chib) ? fb[c] : -INFINITY;
+                        mxb = fmaxf(mxb, fb[c]);
+                    }
+                }
+            }
+            const float za = (mxa == -INFINITY) ? -INFINITY : fmaf(mxa, sc, offa);
+            const float zb = (mxb == -INFINITY) ? -INFINITY : fmaf(mxb, sc, offb);
+            const float mt = fmaxf(za, zb);
+            float corr = 1.f;
+            bool need_o = false;
+            if (mt > m_ref + kRescaleThreshold) {
+                if (m_ref != -INFINITY) {
+                    corr = fast_exp2(m_ref - mt);
+                    need_o = (t > 0);
+                }
+                m_ref = mt;
+            }
+            l *= corr;
+            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+            if (DBG == 1) {
+                const int na = max(0, chia - cloa + 1), nb = max(0, chib - clob + 1);
+                cnt += na + nb;
+                isum += (long long)na * key0a + (long long)(cloa + chia) * na / 2;
+                isum += (long long)nb * key0b + (long long)(clob + chib) * nb / 2;
+            }
+            if (DBG == 2 && row_ok && lse2_in != -INFINITY) {
+                for (int c = 0; c < CHUNK; ++c) {
+                    if (c >= cloa && c <= chia)
+                        args.P[row_g * s.N + key0a + c] = exp2f(fmaf(fa[c], sc, offa - lse2_in));
+                    if (nch > 1 && c >= clob && c <= chib)
+                        args.P[row_g * s.N + key0b + c] = exp2f(fmaf(fb[c], sc, offb - lse2_in));
+                }
+            }
+
+            // P = exp2(z - m_ref) as bf16, written over the chunk's S columns
+            float lsum = 0.f;
+            uint32_t pk[CHUNK / 2];
+            {
+                const float ba = offa - mu;
+#pragma unroll
+                for (int c = 0; c < CHUNK; c += 2) {
+                    const float p0v = fast_exp2(fmaf(fa[c], sc, ba));
+                    const float p1v = fast_exp2(fmaf(fa[c + 1], sc, ba));
+                    lsum += p0v + p1v;
+                    pk[c / 2] = pack_bf16(p0v, p1v);
+                }
+                tmem_st16(tS, pk);
+            }
+            if (nch > 1) {
+                const float bbv = offb - mu;
+#pragma unroll
+                for (int c = 0; c < CHUNK; c += 2) {
+                    const float p0v = fast_exp2(fmaf(fb[c], sc, bbv));
+                    const float p1v = fast_exp2(fmaf(fb[c + 1], sc, bbv));
+                    lsum += p0v + p1v;
+                    pk[c / 2] = pack_bf16(p0v, p1v);
+                }
+                tmem_st16(tS + CHUNK / 2, pk);
+            }
+            l += lsum;
+            __syncwarp();
+
+            // rescale this row of O when the reference max moved (PV of the previous tile done)
+            if (__any_sync(0xffffffffu, need_o)) {
+                ok = wait_bar(bar(C::B_PV), (t - 1) & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const float f = need_o ? corr : 1.f;
+#pragma unroll
+                for (int oc = 0; oc < D / 32; ++oc) {
+                    uint32_t x[32];
+                    tmem_ld32(tbase + lane_base + O_COL + oc * 32, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * f);
+                    tmem_st32(tbase + lane_base + O_COL + oc * 32, x);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PR + buf));
+        }
+
+        // ---- epilogue: O / l -> bf16 -> shared (swizzled, reusing the Q buffer) -> TMA store
+        // A parity wait is exact only if the barrier is at most one phase behind the awaited
+        // one; S of the last tile only guarantees PV of tile n_tiles-3, so step through n_tiles-2.
+        if (ok && n_tiles >= 2) {
+            ok = wait_bar(bar(C::B_PV), (n_tiles - 2) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            ok = wait_bar(bar(C::B_PV), (n_tiles - 1) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        if (ok) {
+            tc_fence_after();
+            __syncwarp();
+#pragma unroll
+            for (int oc = 0; oc < D / 32; ++oc) {
+                uint32_t x[32];
+                tmem_ld32(tbase + lane_base + O_COL + oc * 32, x);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2)
+                    pk[c / 2] = pack_bf16(__uint_as_float(x[c]) * inv_l, __uint_as_float(x[c + 1]) * inv_l);
+                const int dc = oc >> 1, half = oc & 1;
+                uint8_t *rowp = smem + C::Q_OFF + dc * C::Q_DBLK + r * ROW_BYTES;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int cidx = half * 4 + w;
+                    uint4 val = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (r & 7)) << 4)) = val;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (ok && warp == 4 && lane == 0) {
+            for (int dc = 0; dc < C::KD; ++dc)
+                tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0);
+            tma_store_commit_and_wait();
+        }
+        if (ok && row_ok) {
+            args.lse[row_g] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            if (DBG == 1) {
+                args.cnt[row_g] = (int)cnt;
+                args.isum[row_g] = isum;
+            }
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, TMEM_COLS);
+    }
+}
+
+// Bounded-wait self test: waits on a barrier that never completes.
+__global__ void wait_timeout_probe_kernel(int *status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ uint32_t abort_storage;
+    const uint32_t b = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_storage = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        WaitCtx w{&abort_storage, status, timeout_ns};
+        wait_bar(b, 0, w);
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 tensor map over [planes][rows][d] with a (64, box_rows, box_planes) box, 128B swizzle.
+static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long planes, int box_rows,
+                     int box_planes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)rows};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int DBG>
+static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const CUtensorMap &mo, const TcArgs &a, unsigned grid, cudaStream_t st) {
+    constexpr int smem = Cfg<D>::SMEM_BYTES;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, DBG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    fwd_tc_kernel<D, DBG><<<grid, NUM_THREADS, smem, st>>>(mq, mk, mv, mo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
+    using namespace tc;
+    const Shape &s = L.s;
+    const int G = s.H / s.Hkv;
+    const int GP = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+    const int R = BM / GP;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, L.q, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mo, L.out, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
+        !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
+        return cudaErrorNotSupported;
+    TcArgs a{L.alpha, L.lse, s, GP, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P};
+    const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (s.d == 64) {
+        if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        return launch<64, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
+    }
+    if (s.d == 128) {
+        if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        return launch<128, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_timeout_probe(int *status, uint64_t timeout_ns, cudaStream_t st) {
+    tc::wait_timeout_probe_kernel<<<1, 32, 0, st>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace pi

@@ -1,0 +1,51 @@
+// pi_launch.h -- host-side launch descriptors shared by the C ABI and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pi_common.cuh"
+
+namespace pi {
+
+struct LaunchFwd {
+    const void *q, *k, *v;
+    const float *alpha;
+    void *out;
+    float *lse;
+    Shape s;
+    bool fp32;
+    int dbg;               // 0 forward, 1 + counts, 2 + probability dump
+    int *cnt;              // dbg 1
+    long long *isum;       // dbg 1
+    const float *lse_in;   // dbg 2
+    float *P;              // dbg 2
+    int *status;           // device status word
+    uint64_t timeout_ns;   // bound on every device-side wait
+};
+
+struct LaunchBwd {
+    const void *q, *k, *v;
+    const float *alpha;
+    const void *out;
+    const float *lse;
+    const void *dout;
+    void *dq, *dk, *dv;
+    float *dalpha;
+    float *Dws;
+    Shape s;
+    bool fp32;
+};
+
+// CUDA-core kernels (pi_simt.cu)
+cudaError_t launch_fwd_simt(const LaunchFwd &L, cudaStream_t st);
+cudaError_t launch_bwd_simt(const LaunchBwd &L, cudaStream_t st);
+
+// tcgen05 / TMEM / TMA forward, bf16, d in {64, 128} (pi_fwd_tc.cu).
+// Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
+cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st);
+
+// bounded-wait self test (pi_fwd_tc.cu)
+cudaError_t launch_wait_timeout_probe(int *status, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace pi

@@ -1,0 +1,123 @@
+"""Host-only tests of the C ABI: the library builds and loads, exports every
+entry point include/pi_attn.h declares, and rejects bad arguments with the
+documented status code before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from structured_sparse_long_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pi_attn.h")
+
+PI_OK, PI_ERR_NULL, PI_ERR_SHAPE, PI_ERR_UNSUPPORTED, PI_ERR_ALIGN, PI_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    from structured_sparse_long_gb300 import _binding
+    return _binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(pi_attn_[a-z0-9_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
+              "pi_attn_bwd_workspace_size", "pi_attn_status", "pi_attn_strerror",
+              "pi_attn_debug_counts", "pi_attn_debug_probs", "pi_attn_debug_wait_timeout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(pbuild.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_strerror(lib):
+    assert lib.pi_attn_strerror(0) == b"PI_OK"
+    for code in range(-7, 0):
+        assert lib.pi_attn_strerror(code).startswith(b"PI_ERR")
+    assert b"unknown" in lib.pi_attn_strerror(-99)
+
+
+def test_workspace_size(lib):
+    assert lib.pi_attn_bwd_workspace_size(2, 16, 16, 16384, 64) == 2 * 16 * 16384 * 4
+    assert lib.pi_attn_bwd_workspace_size(1, 1, 1, 3, 64) == 256
+    assert lib.pi_attn_bwd_workspace_size(0, 1, 1, 3, 64) == 0
+
+
+A16 = 0x10000  # fake, 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd_call(lib, q=A16, k=A16, v=A16, alpha=A16, B=1, H=2, Hkv=2, N=64, d=64, kl=8, per=16, S=1,
+             mode=0, out=A16, lse=A16, fn="pi_attn_fwd"):
+    return getattr(lib, fn)(q, k, v, alpha, B, H, Hkv, N, d, kl, per, S, mode, out, lse, None)
+
+
+@pytest.mark.parametrize("fn", ["pi_attn_fwd", "pi_attn_fwd_f32"])
+def test_fwd_validation(lib, fn):
+    assert fwd_call(lib, q=None, fn=fn) == PI_ERR_NULL
+    assert fwd_call(lib, out=None, fn=fn) == PI_ERR_NULL
+    assert fwd_call(lib, lse=None, fn=fn) == PI_ERR_NULL
+    assert fwd_call(lib, alpha=None, fn=fn) == PI_ERR_NULL          # pi mode needs alpha
+    assert fwd_call(lib, B=0, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, N=-1, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, H=3, Hkv=2, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, kl=-1, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, S=-1, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, per=0, S=2, fn=fn) == PI_ERR_SHAPE
+    assert fwd_call(lib, mode=1, kl=0, S=0, alpha=None, fn=fn) == PI_ERR_SHAPE   # ECP needs c > 0
+    assert fwd_call(lib, mode=1, kl=16, S=1, fn=fn) == PI_ERR_SHAPE               # ECP has no skip
+    assert fwd_call(lib, d=48, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, d=256, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, mode=2, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, B=1 << 12, H=1 << 10, Hkv=1 << 10, N=1 << 10, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, q=A16 + 8, fn=fn) == PI_ERR_ALIGN
+    assert fwd_call(lib, v=A16 + 2, fn=fn) == PI_ERR_ALIGN
+    assert fwd_call(lib, out=A16 + 4, fn=fn) == PI_ERR_ALIGN
+    assert fwd_call(lib, lse=A16 + 2, fn=fn) == PI_ERR_ALIGN
+
+
+def bwd_call(lib, ws=A16, ws_bytes=1 << 20, dq=A16, alpha=A16, d=64, dalpha=A16, N=64, fn="pi_attn_bwd"):
+    return getattr(lib, fn)(A16, A16, A16, alpha, A16, A16, A16, 1, 2, 2, N, d, 8, 16, 1, 0,
+                            dq, A16, A16, dalpha, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("fn", ["pi_attn_bwd", "pi_attn_bwd_f32"])
+def test_bwd_validation(lib, fn):
+    assert bwd_call(lib, dq=None, fn=fn) == PI_ERR_NULL
+    assert bwd_call(lib, alpha=None, fn=fn) == PI_ERR_NULL
+    assert bwd_call(lib, d=16, fn=fn) == PI_ERR_UNSUPPORTED
+    assert bwd_call(lib, dq=A16 + 8, fn=fn) == PI_ERR_ALIGN
+    assert bwd_call(lib, dalpha=A16 + 1, fn=fn) == PI_ERR_ALIGN
+    assert bwd_call(lib, ws=None, fn=fn) == PI_ERR_WORKSPACE
+    assert bwd_call(lib, ws_bytes=16, fn=fn) == PI_ERR_WORKSPACE
+
+
+def test_debug_validation(lib):
+    assert lib.pi_attn_debug_counts(A16, A16, A16, A16, 1, 2, 2, 64, 64, 8, 16, 1, 0, 0, A16, A16,
+                                    None, A16, None) == PI_ERR_NULL
+    assert lib.pi_attn_debug_counts(A16, A16, A16, A16, 1, 2, 2, 64, 64, 8, 16, 1, 0, 5, A16, A16,
+                                    A16, A16, None) == PI_ERR_UNSUPPORTED
+    assert lib.pi_attn_debug_probs(A16, A16, A16, A16, A16, 1, 2, 2, 4096, 64, 8, 16, 1, 0, 0, A16,
+                                   A16, A16, None) == PI_ERR_UNSUPPORTED
+    assert lib.pi_attn_debug_wait_timeout(0, None) == PI_ERR_SHAPE
+
+
+def test_binding_fails_loudly_without_cuda():
+    """The product path has no CPU fallback: CPU tensors are rejected."""
+    import torch
+    import structured_sparse_long_gb300 as pa
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError)):
+        pa.fwd(q, q, q, torch.ones(1, 2, 8), 4, 8, 1)

@@ -1,0 +1,57 @@
+"""World-size-2 gloo tests (CPU) of the benchmark's multi-rank host logic: the job is
+timed by its slowest rank, and the reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        got = bench.reduce_max(10.0 + rank * 5.0, world, "cpu")
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_reference_arm_silent_off_rank0(capsys):
+    import bench
+
+    class A:
+        warmup, steps, gpus = 3, 1, 2
+    bench.reference_arm(A, bench.WORKLOADS["C1"], rank=1, world=2)
+    assert capsys.readouterr().out == ""
+
+
+def test_work_accounting_matches_closed_forms():
+    import bench
+    w = bench.WORKLOADS["C4"]
+    wk = bench.work(w, False)
+    assert wk["pairs"] == 17061760 * 16
+    assert wk["fwd_bytes"] == 2 * 268435456 + 2 * 67108864 + 2 * 4 * 16 * 65536
+    assert bench.pairs_per_head(8192, 512, 0, 0, 1) == 6033408
