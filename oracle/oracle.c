@@ -113,22 +113,20 @@ void oracle_counts(long N, int mode, long k_local, long period, int S,
     }
 }
 
-/* Logits, softmax and output of one row.  z and p have room for cap entries.
-   Writes out_row[d] and returns lse. */
-static double one_row(const void *q, const void *k, const void *v, int dt,
-                      const float *alpha, long B_, long H, long Hkv, long N, long d,
-                      int mode, long b, long h, long i, long n, const long *idx,
-                      const int *tag, double *z, double *p, double *out_row) {
-    (void)B_;
+/* Logits, softmax and output of one row (inputs already widened to fp64).
+   z and p have room for n entries.  Writes out_row[d] and returns lse. */
+static double one_row(const double *q, const double *k, const double *v, const float *alpha,
+                      long H, long Hkv, long N, long d, int mode, long b, long h, long i, long n,
+                      const long *idx, const int *tag, double *z, double *p, double *out_row) {
     long g = h / (H / Hkv);
-    size_t qoff = (((size_t)b * H + h) * N + i) * d;
+    const double *qrow = q + (((size_t)b * H + h) * N + i) * d;
     double a = alpha ? (double)alpha[((size_t)b * H + h) * N + i] : 1.0;
     double scale = 1.0 / sqrt((double)d);
     double M = -INFINITY;
     for (long t = 0; t < n; ++t) {
-        size_t koff = (((size_t)b * Hkv + g) * N + idx[t]) * d;
+        const double *krow = k + (((size_t)b * Hkv + g) * N + idx[t]) * d;
         double dot = 0.0;
-        for (long c = 0; c < d; ++c) dot += ld(q, dt, qoff + c) * ld(k, dt, koff + c);
+        for (long c = 0; c < d; ++c) dot += qrow[c] * krow[c];
         double prior = 0.0;
         if (mode == MODE_PI) prior = (tag[t] == 0) ? log(a) : log1p(-a);
         z[t] = dot * scale + prior;
@@ -143,10 +141,19 @@ static double one_row(const void *q, const void *k, const void *v, int dt,
     for (long t = 0; t < n; ++t) l += exp(z[t] - M);
     for (long t = 0; t < n; ++t) p[t] = exp(z[t] - M) / l;
     for (long t = 0; t < n; ++t) {
-        size_t voff = (((size_t)b * Hkv + g) * N + idx[t]) * d;
-        for (long c = 0; c < d; ++c) out_row[c] += p[t] * ld(v, dt, voff + c);
+        const double *vrow = v + (((size_t)b * Hkv + g) * N + idx[t]) * d;
+        for (long c = 0; c < d; ++c) out_row[c] += p[t] * vrow[c];
     }
     return M + log(l);
+}
+
+/* Widen an input tensor of n elements to fp64 (exact for fp32 and bf16). */
+static double *widen(const void *x, int dt, size_t n) {
+    double *w = (double *)malloc(sizeof(double) * (n ? n : 1));
+    if (!w) return NULL;
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < (long)n; ++e) w[e] = ld(x, dt, (size_t)e);
+    return w;
 }
 
 /*
@@ -167,6 +174,10 @@ int oracle_fwd(const void *q, const void *k, const void *v, int dt, const float 
     long rows = i_end - i_begin;
     long cap = max_neighbours(N, mode, k_local, S);
     long total = B * H * rows;
+    double *qd = widen(q, dt, (size_t)B * H * N * d);
+    double *kd = widen(k, dt, (size_t)B * Hkv * N * d);
+    double *vd = widen(v, dt, (size_t)B * Hkv * N * d);
+    if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -2; }
 #pragma omp parallel
     {
         long *idx = (long *)malloc(sizeof(long) * cap);
@@ -180,8 +191,8 @@ int oracle_fwd(const void *q, const void *k, const void *v, int dt, const float 
             long i = i_begin + r % rows;
             long n = neighbours(i, mode, k_local, period, S, idx, tag);
             double *orow = out + (size_t)r * d;
-            lse[r] = one_row(q, k, v, dt, alpha, B, H, Hkv, N, d, mode, b, h, i, n, idx, tag,
-                             z, p, orow);
+            lse[r] = one_row(qd, kd, vd, alpha, H, Hkv, N, d, mode, b, h, i, n, idx, tag, z, p,
+                             orow);
             if (P) {
                 double *prow = P + (((size_t)b * H + h) * N + i) * N;
                 for (long j = 0; j < N; ++j) prow[j] = 0.0;
@@ -190,6 +201,7 @@ int oracle_fwd(const void *q, const void *k, const void *v, int dt, const float 
         }
         free(idx); free(tag); free(z); free(p);
     }
+    free(qd); free(kd); free(vd);
     return 0;
 }
 
@@ -210,6 +222,11 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
     double scale = 1.0 / sqrt((double)d);
     memset(dk, 0, sizeof(double) * (size_t)B * Hkv * N * d);
     memset(dv, 0, sizeof(double) * (size_t)B * Hkv * N * d);
+    double *qd = widen(q, dt, (size_t)B * H * N * d);
+    double *kd = widen(k, dt, (size_t)B * Hkv * N * d);
+    double *vd = widen(v, dt, (size_t)B * Hkv * N * d);
+    double *gd = widen(dout, dt, (size_t)B * H * N * d);
+    if (!qd || !kd || !vd || !gd) { free(qd); free(kd); free(vd); free(gd); return -2; }
 #pragma omp parallel
     {
         long *idx = (long *)malloc(sizeof(long) * cap);
@@ -222,28 +239,30 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
             long b = bg / Hkv, g = bg % Hkv;
             double *dkg = dk + (size_t)bg * N * d;
             double *dvg = dv + (size_t)bg * N * d;
+            const double *kg = kd + (size_t)bg * N * d;
+            const double *vg = vd + (size_t)bg * N * d;
             for (long h = g * G; h < (g + 1) * G; ++h) {
                 for (long i = 0; i < N; ++i) {
                     long n = neighbours(i, mode, k_local, period, S, idx, tag);
-                    one_row(q, k, v, dt, alpha, B, H, Hkv, N, d, mode, b, h, i, n, idx, tag,
-                            z, p, orow);
+                    one_row(qd, kd, vd, alpha, H, Hkv, N, d, mode, b, h, i, n, idx, tag, z, p, orow);
                     size_t qoff = (((size_t)b * H + h) * N + i) * d;
+                    const double *qrow = qd + qoff;
+                    const double *grow = gd + qoff;
                     double D = 0.0;
-                    for (long c = 0; c < d; ++c) D += ld(dout, dt, qoff + c) * orow[c];
+                    for (long c = 0; c < d; ++c) D += grow[c] * orow[c];
                     double *dqrow = dq + qoff;
                     for (long c = 0; c < d; ++c) dqrow[c] = 0.0;
                     double sum_local = 0.0, sum_skip = 0.0;
                     for (long t = 0; t < n; ++t) {
                         size_t koff = (size_t)idx[t] * d;
-                        size_t kvoff = (((size_t)b * Hkv + g) * N + idx[t]) * d;
                         double dp = 0.0;
-                        for (long c = 0; c < d; ++c) dp += ld(dout, dt, qoff + c) * ld(v, dt, kvoff + c);
+                        for (long c = 0; c < d; ++c) dp += grow[c] * vg[koff + c];
                         double dz = p[t] * (dp - D);
                         if (tag[t] == 0) sum_local += dz; else sum_skip += dz;
                         for (long c = 0; c < d; ++c) {
-                            dqrow[c] += dz * ld(k, dt, kvoff + c) * scale;
-                            dkg[koff + c] += dz * ld(q, dt, qoff + c) * scale;
-                            dvg[koff + c] += p[t] * ld(dout, dt, qoff + c);
+                            dqrow[c] += dz * kg[koff + c] * scale;
+                            dkg[koff + c] += dz * qrow[c] * scale;
+                            dvg[koff + c] += p[t] * grow[c];
                         }
                     }
                     if (dalpha) {
@@ -260,5 +279,6 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
         }
         free(idx); free(tag); free(z); free(p); free(orow);
     }
+    free(qd); free(kd); free(vd); free(gd);
     return 0;
 }
