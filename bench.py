@@ -435,6 +435,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
+    ap.add_argument("--seq", type=int, default=0,
+                    help="override the sequence length N (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -443,6 +445,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = WORKLOADS[args.config]
+    if args.seq:
+        w = w.replace(N=args.seq, name=f"{w.name}-N{args.seq}",
+                      description=w.description + f" (N overridden to {args.seq})")
     if args.impl == "reference":
         reference_arm(args, w, rank, world)
         return

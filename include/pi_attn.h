@@ -110,7 +110,9 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
 
 /*
  * pi_attn_bwd_workspace_size -- bytes of device workspace pi_attn_bwd needs
- * for these sizes (one fp32 per query row for D_i = dout_i . out_i).
+ * for these sizes: one fp32 per query row for D_i = sum_j p_ij (dout_i . v_j),
+ * which equals dout_i . out_i in exact arithmetic; it is recomputed from the
+ * probabilities rather than read from the bf16-rounded out.
  */
 size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
 
@@ -118,13 +120,14 @@ size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * pi_attn_bwd -- backward of pi_attn_fwd (the chain rule through the
  * definition above; bf16 tensors, fp32 accumulation).
  *   Inputs: q, k, v, alpha as for the forward; out [B,H,N,d] and lse [B,H,N]
- *   from pi_attn_fwd; dout [B,H,N,d].
+ *   from pi_attn_fwd (out is validated but not read: D_i is recomputed from the
+ *   probabilities); dout [B,H,N,d].
  *   Outputs: dq [B,H,N,d], dk and dv [B,Hkv,N,d] (summed over the query heads
  *   of each KV group) bf16; dalpha [B,H,N] fp32 (may be NULL; zero in ECP mode),
  *   computed as dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)),
  *   which equals sum_L dz/alpha - sum_P dz/(1-alpha) because every softmax row
  *   of dz sums to zero; it is undefined for alpha_i in {0, 1} when P(i) is not
- *   empty.  dz_ij = p_ij (dout_i . v_j - dout_i . out_i).
+ *   empty.  dz_ij = p_ij (dout_i . v_j - D_i), D_i = sum_j p_ij (dout_i . v_j).
  *   workspace: device buffer of at least pi_attn_bwd_workspace_size() bytes,
  *   owned by the caller, contents ignored on entry.  Deterministic.
  */

@@ -64,7 +64,8 @@ struct Cfg {
     static constexpr int B_SF = B_VE + STAGES;
     static constexpr int B_PR = B_SF + 2;
     static constexpr int B_PV = B_PR + 2;
-    static constexpr int B_DR = B_PV + 1;
+    static constexpr int B_OF = B_PV + 1;  // O complete (after the last PV), single phase
+    static constexpr int B_DR = B_OF + 1;
     static constexpr int NBARS = B_DR + 1;
     static constexpr int MISC_BYTES = NBARS * 8 + 16;
     static constexpr int SMEM_BYTES = BAR_OFF + MISC_BYTES + 1024;  // + alignment slack
@@ -349,6 +350,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(bar(C::B_PR + i), 128);
         }
         mbar_init(bar(C::B_PV), 1);
+        mbar_init(bar(C::B_OF), 1);
         mbar_init(bar(C::B_DR), 1);
         *abort_flag = 0u;
         fence_barrier_init();
@@ -459,6 +461,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     tc_commit(bar(C::B_PV));
                     tc_commit(bar(C::B_VE + st));
+                    if (u == n_tiles - 1) tc_commit(bar(C::B_OF));
                 }
             }
             // every MMA issued so far has finished before TMEM is released
@@ -609,7 +612,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             l += lsum;
             __syncwarp();
 
-            // rescale this row of O when the reference max moved (PV of the previous tile done)
+            // Rescale this row of O when the reference max moved.  PV of tile t-1 must be done.
+            // The wait names that phase exactly: S of tile t implies PV of tile t-2 finished,
+            // and PV of tile t cannot start before this thread arrives below.
             if (__any_sync(0xffffffffu, need_o)) {
                 ok = wait_bar(bar(C::B_PV), (t - 1) & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -632,14 +637,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
 
         // ---- epilogue: O / l -> bf16 -> shared (swizzled, reusing the Q buffer) -> TMA store
-        // A parity wait is exact only if the barrier is at most one phase behind the awaited
-        // one; S of the last tile only guarantees PV of tile n_tiles-3, so step through n_tiles-2.
-        if (ok && n_tiles >= 2) {
-            ok = wait_bar(bar(C::B_PV), (n_tiles - 2) & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-        }
+        // A parity wait names a phase only if the barrier is at most one phase away from it;
+        // by now the PV barrier may be anywhere from n_tiles-2 to n_tiles phases along, so the
+        // epilogue waits on its own single-phase barrier.
         if (ok) {
-            ok = wait_bar(bar(C::B_PV), (n_tiles - 1) & 1, wc);
+            ok = wait_bar(bar(C::B_OF), 0, wc);
             ok = __all_sync(0xffffffffu, ok);
         }
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

@@ -10,7 +10,7 @@
 // log2(1 - alpha) instead of log2(alpha).
 //
 // Backward (chain rule through the same definition):
-//   D_i = dout_i . out_i
+//   D_i = sum_j p_ij (dout_i . v_j)   (= dout_i . out_i in exact arithmetic)
 //   dz_ij = p_ij (dout_i . v_j - D_i),  p_ij = exp(z_ij - lse_i)
 //   dq_i = sum_j dz_ij k_j / sqrt(d)            (query-major kernel)
 //   dk_j = sum_{h in group} sum_i dz_ij q_i / sqrt(d),  dv_j = sum p_ij dout_i
@@ -166,20 +166,11 @@ struct BwdArgs {
     float *Dws;  // [B*H*N]
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) bwd_prep_kernel(BwdArgs a, long long rows) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * kWarps + warp;
-    if (row >= rows) return;
-    const T *o = static_cast<const T *>(a.out) + row * D;
-    const T *g = static_cast<const T *>(a.dout) + row * D;
-    float acc = 0.f;
-    for (int c = lane; c < D; c += 32) acc = fmaf(to_f32(o[c]), to_f32(g[c]), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) a.Dws[row] = acc;
-}
-
-// one warp per query row: dq and dalpha
+// One warp per query row: D_i, dq and dalpha in one pass over the row's keys.
+// D_i = sum_j p_ij dp_ij (equal to dout_i . out_i in exact arithmetic, but free of
+// the rounding of the stored bf16 out, which 1/(alpha(1-alpha)) would amplify in
+// dalpha); dq_i = tau (sum_j p dp k_j - D_i sum_j p k_j) = tau sum_j dz_ij k_j.
+// D_i is written to the workspace for the key-major pass.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s) {
     __shared__ __align__(16) float qs[kWarps][D];
@@ -206,30 +197,35 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
     const float off_b = (s.mode == 0) ? log2f(al) : 0.f;
     const float off_s = log2f(1.f - al);
     const float lse2 = a.lse[row] * kLog2e;
-    const float Drow = a.Dws[row];
     constexpr int RC = D / 32;
-    float acc[RC];
+    float acc_pdk[RC], acc_pk[RC];
 #pragma unroll
-    for (int r = 0; r < RC; ++r) acc[r] = 0.f;
-    float skip_dz = 0.f;
+    for (int r = 0; r < RC; ++r) { acc_pdk[r] = 0.f; acc_pk[r] = 0.f; }
+    float d_part = 0.f, skip_p = 0.f, skip_pdp = 0.f;
     bool any_skip = false;
 
     auto chunk = [&](int j, bool valid, float off, bool is_skip) {
-        float dz = 0.f;
+        float p = 0.f, dp = 0.f;
         if (valid && lse2 != -INFINITY) {
             const float z = fmaf(dot_row<T, D>(qs[warp], kb + (long long)j * D), s.scale_log2, off);
-            const float p = exp2f(z - lse2);
-            const float dp = dot_row<T, D>(gs[warp], vb + (long long)j * D);
-            dz = p * (dp - Drow);
+            p = exp2f(z - lse2);
+            dp = dot_row<T, D>(gs[warp], vb + (long long)j * D);
         }
-        if (is_skip) skip_dz += dz;
+        const float pdp = p * dp;
+        d_part += pdp;
+        if (is_skip) { skip_p += p; skip_pdp += pdp; }
         for (int c = 0; c < 32; ++c) {
-            const float dzc = __shfl_sync(kFull, dz, c);
+            const float pc = __shfl_sync(kFull, p, c);
+            const float pdc = __shfl_sync(kFull, pdp, c);
             const int jc = __shfl_sync(kFull, j, c);
-            if (dzc != 0.f) {
+            if (pc != 0.f) {
                 const T *kr = kb + (long long)jc * D;
 #pragma unroll
-                for (int r = 0; r < RC; ++r) acc[r] = fmaf(dzc, to_f32(kr[lane + 32 * r]), acc[r]);
+                for (int r = 0; r < RC; ++r) {
+                    const float kv = to_f32(kr[lane + 32 * r]);
+                    acc_pk[r] = fmaf(pc, kv, acc_pk[r]);
+                    acc_pdk[r] = fmaf(pdc, kv, acc_pdk[r]);
+                }
             }
         }
     };
@@ -249,14 +245,19 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
             chunk(valid ? (int)jj : 0, valid, off_s, true);
         }
     }
+    const float Drow = warp_sum(d_part);
     const float scale = s.scale_log2 / kLog2e;  // 1/sqrt(d)
     T *dqrow = static_cast<T *>(a.dq) + row * D;
 #pragma unroll
-    for (int r = 0; r < RC; ++r) dqrow[lane + 32 * r] = from_f32<T>(acc[r] * scale);
-    skip_dz = warp_sum(skip_dz);
+    for (int r = 0; r < RC; ++r)
+        dqrow[lane + 32 * r] = from_f32<T>((acc_pdk[r] - Drow * acc_pk[r]) * scale);
+    const float sdz = warp_sum(skip_pdp) - Drow * warp_sum(skip_p);  // sum over P(i) of dz
     any_skip = __any_sync(kFull, any_skip);
-    if (lane == 0 && a.dalpha)
-        a.dalpha[row] = (s.mode == 0 && any_skip) ? -skip_dz / (al * (1.f - al)) : 0.f;
+    if (lane == 0) {
+        a.Dws[row] = Drow;
+        if (a.dalpha)
+            a.dalpha[row] = (s.mode == 0 && any_skip) ? -sdz / (al * (1.f - al)) : 0.f;
+    }
 }
 
 // one warp per key row (b, g, j): dk and dv, summed over the query heads of group g
@@ -373,7 +374,6 @@ static cudaError_t bwd_run(const BwdArgs &a, const Shape &s, cudaStream_t st) {
     const long long krows = (long long)s.B * s.Hkv * s.N;
     const dim3 g1((unsigned)((rows + kWarps - 1) / kWarps));
     const dim3 g2((unsigned)((krows + kWarps - 1) / kWarps));
-    bwd_prep_kernel<T, D><<<g1, kWarps * 32, 0, st>>>(a, rows);
     bwd_dq_kernel<T, D><<<g1, kWarps * 32, 0, st>>>(a, s);
     bwd_dkdv_kernel<T, D><<<g2, kWarps * 32, 0, st>>>(a, s);
     return cudaGetLastError();

@@ -142,6 +142,7 @@ def test_counts_bit_exact(spec):
     _, _, cnt, isum = pa.debug_counts(dev["q"], dev["k"], dev["v"], dev["alpha"], w.k_local,
                                       w.period, w.S, w.mode)
     torch.cuda.synchronize()
+    assert pa.status() == 0
     rc, ri = oracle.counts(w.N, w.k_local, w.period, w.S, w.mode)
     exp_c = np.broadcast_to(rc, (w.B, w.H, w.N))
     exp_i = np.broadcast_to(ri, (w.B, w.H, w.N))
@@ -157,6 +158,7 @@ def test_workload_counts_bit_exact(name):
     _, _, cnt, isum = pa.debug_counts(dev["q"], dev["k"], dev["v"], dev["alpha"], w.k_local,
                                       w.period, w.S, w.mode)
     torch.cuda.synchronize()
+    assert pa.status() == 0
     rc, ri = oracle.counts(w.N, w.k_local, w.period, w.S, w.mode)
     c = cnt.cpu().numpy()
     s = isum.cpu().numpy()
@@ -176,6 +178,7 @@ def test_probability_dump(spec):
     P = pa.debug_probs(dev["q"], dev["k"], dev["v"], dev["alpha"], lse, w.k_local, w.period, w.S,
                        w.mode)
     torch.cuda.synchronize()
+    assert pa.status() == 0
     _, _, Pref = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["alpha"], w.k_local, w.period, w.S,
                             w.mode, want_P=True)
     Pg = P.cpu().numpy()
