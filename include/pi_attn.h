@@ -145,6 +145,38 @@ int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *al
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pi_attn_bwd_noalloc -- the bf16 backward of pi_attn_bwd, for callers that
+ * cannot hand the library a workspace and must not allocate device memory
+ * themselves.  The paper has no counterpart to this entry point; it exists
+ * for deployment.  Examples of such callers: a serving runtime that reserved
+ * the device memory up front for its own pool, where a cudaMalloc would fail
+ * or fragment that reservation; code on a latency-critical path, where
+ * cudaFree's implicit device-wide synchronisation is not acceptable; and
+ * language bindings that only forward the buffers they were given.
+ *
+ * Arguments, layouts and results are those of pi_attn_bwd without the
+ * workspace.  The scratch memory (one fp32 per query row) is a fixed
+ * file-scope device array of PI_ATTN_NOALLOC_MAX_ROWS floats (4 MiB), which
+ * every GPU that loads the library holds until the process exits.
+ *   - B*H*N above PI_ATTN_NOALLOC_MAX_ROWS returns PI_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - The first call on each device looks up that device's address of the
+ *     array (cudaGetSymbolAddress, with the device current) and caches it;
+ *     make that first call before any stream capture.  It never calls
+ *     cudaMalloc, cudaFree or any allocating routine.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     Nothing in it has to start at zero: each call writes every entry it
+ *     reads.  Calls whose kernels overlap on the GPU (different streams
+ *     without ordering between them) race on the array and give undefined
+ *     results; order them on one stream or with events.
+ */
+#define PI_ATTN_NOALLOC_MAX_ROWS (1 << 20)
+int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float *alpha,
+                        const void *out, const float *lse, const void *dout,
+                        int B, int H, int Hkv, int N, int d, int k_local, int period, int S,
+                        int mode, void *dq, void *dk, void *dv, float *dalpha, void *stream);
+
+/*
  * pi_attn_status -- synchronises `stream`, reads the current device's status
  * word, resets it to PI_OK and returns what it held (PI_OK or
  * PI_ERR_DEVICE_TIMEOUT), or PI_ERR_CUDA if the synchronisation failed.

@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
         bwd_args = [P, P, P, P, P, P, P] + [I] * 9 + [P, P, P, P, P, Z, P]
         lib.pi_attn_bwd.argtypes = bwd_args
         lib.pi_attn_bwd_f32.argtypes = bwd_args
+        lib.pi_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P] + [I] * 9 + [P, P, P, P, P]
+        lib.pi_attn_bwd_noalloc.restype = I
         lib.pi_attn_bwd_workspace_size.argtypes = [I] * 5
         lib.pi_attn_bwd_workspace_size.restype = Z
         lib.pi_attn_status.argtypes = [P]
@@ -165,6 +167,30 @@ def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode:
             B, H, Hkv, N, d, k_local, period, S, mode, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(fn.__name__, rc)
+    return dq, dk, dv, dalpha
+
+
+def bwd_noalloc(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int,
+                mode: int = MODE_PI, dq=None, dk=None, dv=None, dalpha=None, stream=None):
+    """pi_attn_bwd_noalloc (bf16): the backward with the library's fixed device scratch
+    instead of a caller workspace.  Returns (dq, dk, dv, dalpha)."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    for t, n in ((q, "q"), (out, "out"), (dout, "dout")):
+        _expect(t, n, torch.bfloat16, q.shape)
+    for t, n in ((k, "k"), (v, "v")):
+        _expect(t, n, torch.bfloat16, k.shape)
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H, N))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dalpha is None:
+        dalpha = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    rc = load().pi_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse),
+                                    _ptr(dout), B, H, Hkv, N, d, k_local, period, S, mode,
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _stream(stream))
+    _check("pi_attn_bwd_noalloc", rc)
     return dq, dk, dv, dalpha
 
 

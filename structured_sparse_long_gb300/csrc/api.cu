@@ -112,6 +112,29 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
 
 }  // namespace
 
+// Scratch of pi_attn_bwd_noalloc: one fp32 per query row, fixed size, shared by every call
+// on a device.  In host code the name is only a host-side stand-in; kernels get the
+// device address from noalloc_scratch().
+static __device__ __align__(256) float g_noalloc_scratch[PI_ATTN_NOALLOC_MAX_ROWS];
+
+namespace {
+
+// Device address of g_noalloc_scratch for the current device, looked up once per device.
+float *noalloc_scratch() {
+    static float *cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!cache[dev]) {
+        float *p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_scratch) != cudaSuccess)
+            return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 int pi_attn_fwd(const void *q, const void *k, const void *v, const float *alpha, int B, int H, int Hkv,
@@ -150,6 +173,20 @@ int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *al
                     float *dalpha, void *workspace, size_t workspace_bytes, void *stream) {
     return run_bwd(q, k, v, alpha, out, lse, dout, B, H, Hkv, N, d, k_local, period, S, mode, dq, dk,
                    dv, dalpha, workspace, workspace_bytes, stream, true);
+}
+
+int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float *alpha,
+                        const void *out, const float *lse, const void *dout, int B, int H, int Hkv,
+                        int N, int d, int k_local, int period, int S, int mode, void *dq, void *dk,
+                        void *dv, float *dalpha, void *stream) {
+    const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    if (rc != PI_OK) return rc;
+    if ((long long)B * H * N > (long long)PI_ATTN_NOALLOC_MAX_ROWS) return PI_ERR_WORKSPACE;
+    float *scratch = noalloc_scratch();
+    if (!scratch) return PI_ERR_CUDA;
+    return run_bwd(q, k, v, alpha, out, lse, dout, B, H, Hkv, N, d, k_local, period, S, mode, dq, dk,
+                   dv, dalpha, scratch, sizeof(float) * (size_t)PI_ATTN_NOALLOC_MAX_ROWS, stream,
+                   false);
 }
 
 int pi_attn_status(void *stream) {
