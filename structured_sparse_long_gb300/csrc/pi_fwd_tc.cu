@@ -137,10 +137,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
+// Same with an L2 cache policy (createpolicy) attached to the transfer.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int x, int y, int z,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+        "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 __device__ __forceinline__ void tma_store_commit_and_wait() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -204,6 +226,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
         : PI_R8(0), PI_R8(8), PI_R8(16), PI_R8(24)
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : PI_R8(0), PI_R8(8)
+        : "r"(taddr));
+}
 #undef PI_R8
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -229,6 +258,94 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction for two lanes of work).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// f[x] for a runtime index x in [0, 32) without local memory: a select tree on x's bits.
+__device__ __forceinline__ float select32(const float *f, int x) {
+    float a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = (x & 1) ? f[2 * j + 1] : f[2 * j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = (x & 2) ? a[2 * j + 1] : a[2 * j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = (x & 4) ? b[2 * j + 1] : b[2 * j];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) d[j] = (x & 8) ? c[2 * j + 1] : c[2 * j];
+    return (x & 16) ? d[1] : d[0];
+}
+
+// Phase 1 of a key chunk for one row: mask the scores outside [clo, chi] and return the
+// chunk's largest logit in log2 units (prior included).  A skip chunk holds at most one
+// valid column per row (its diagonal), read with a select tree instead of a full pass.
+__device__ __forceinline__ float chunk_max(float *f, int clo, int chi, bool skip, float sc, float off) {
+    if (skip) {
+        if (clo > chi) return -INFINITY;
+        return fmaf(select32(f, clo), sc, off);
+    }
+    float mx = -INFINITY;
+    if (!__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) f[c] = (c >= clo && c <= chi) ? f[c] : -INFINITY;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) mx = max3(mx, f[c], f[c + 1]);
+    return (mx == -INFINITY) ? -INFINITY : fmaf(mx, sc, off);
+}
+
+// Phase 2: P = exp2(logit - mu) packed as 16 bf16 pairs; returns the chunk's sum of P.
+// For a skip chunk `zdiag` is the diagonal logit from phase 1 and column clo the only
+// non-zero entry.
+__device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, float zdiag, float sc,
+                                           float off, float mu, uint32_t *pk) {
+    if (skip) {
+        const float p = fast_exp2(zdiag - mu);
+        __nv_bfloat16 hb = __float2bfloat16_rn(p);
+        const uint32_t bits = (uint32_t)(*reinterpret_cast<uint16_t *>(&hb));
+        const uint32_t word = (clo & 1) ? (bits << 16) : bits;
+#pragma unroll
+        for (int w = 0; w < 16; ++w) pk[w] = (w == (clo >> 1)) ? word : 0u;
+        return p;
+    }
+    const float bo = off - mu;
+    const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo);
+    uint64_t acc = pack2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+        float z0, z1;
+        unpack2(fma2(pack2(f[c], f[c + 1]), sc2, bo2), z0, z1);
+        const float p0 = fast_exp2(z0);
+        const float p1 = fast_exp2(z1);
+        acc = add2(acc, pack2(p0, p1));
+        pk[c / 2] = pack_bf16(p0, p1);
+    }
+    float a0, a1;
+    unpack2(acc, a0, a1);
+    return a0 + a1;
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
@@ -366,9 +483,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
+            const uint64_t stream_once = policy_evict_first(), reused = policy_evict_last();
             mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
             for (int dc = 0; dc < C::KD; ++dc)
-                tma_load_3d(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q));
+                tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
+                                 stream_once);
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
@@ -380,8 +499,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     bool sk;
                     const int key0 = cw.key0(2 * t + cc, back, u, sk);
                     for (int dc = 0; dc < C::KD; ++dc)
-                        tma_load_3d(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
-                                    dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st));
+                        tma_load_3d_hint(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
+                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st), reused);
                 }
                 issued = t + 1;
             }
@@ -397,6 +516,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ================= producer: V tiles
         if (lane == 0) {
             prefetch_tmap(&tmV);
+            const uint64_t reused = policy_evict_last();
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
@@ -408,8 +528,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     bool sk;
                     const int key0 = cw.key0(2 * t + cc, back, u, sk);
                     for (int dc = 0; dc < C::KD; ++dc)
-                        tma_load_3d(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
-                                    dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st));
+                        tma_load_3d_hint(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
+                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st), reused);
                 }
                 issued = t + 1;
             }
@@ -493,9 +613,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bool ok = true;
 
         // valid column range [clo, chi] of chunk ci for this row, and its prior
-        auto chunk_range = [&](int ci, int &key0, int &clo, int &chi, float &off) {
+        auto chunk_range = [&](int ci, int &key0, int &clo, int &chi, float &off, bool &sk) {
             int back, u;
-            bool sk;
             key0 = cw.key0(ci, back, u, sk);
             if (!sk) {
                 clo = max(lo_i - key0, 0);
@@ -526,36 +645,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
             int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
             float offa, offb = 0.f;
-            chunk_range(2 * t, key0a, cloa, chia, offa);
-            if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb);
+            bool ska, skb = false;
+            chunk_range(2 * t, key0a, cloa, chia, offa, ska);
+            if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb, skb);
 
             float *fa = reinterpret_cast<float *>(ra);
             float *fb = reinterpret_cast<float *>(rb);
-            float mxa = -INFINITY, mxb = -INFINITY;
-            if (__all_sync(0xffffffffu, cloa <= 0 && chia >= CHUNK - 1)) {
-#pragma unroll
-                for (int c = 0; c < CHUNK; ++c) mxa = fmaxf(mxa, fa[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < CHUNK; ++c) {
-                    fa[c] = (c >= cloa && c <= chia) ? fa[c] : -INFINITY;
-                    mxa = fmaxf(mxa, fa[c]);
-                }
-            }
-            if (nch > 1) {
-                if (__all_sync(0xffffffffu, clob <= 0 && chib >= CHUNK - 1)) {
-#pragma unroll
-                    for (int c = 0; c < CHUNK; ++c) mxb = fmaxf(mxb, fb[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < CHUNK; ++c) {
-                        fb[c] = (c >= clob && c <= chib) ? fb[c] : -INFINITY;
-                        mxb = fmaxf(mxb, fb[c]);
-                    }
-                }
-            }
-            const float za = (mxa == -INFINITY) ? -INFINITY : fmaf(mxa, sc, offa);
-            const float zb = (mxb == -INFINITY) ? -INFINITY : fmaf(mxb, sc, offb);
+            const float za = chunk_max(fa, cloa, chia, ska, sc, offa);
+            const float zb = (nch > 1) ? chunk_max(fb, clob, chib, skb, sc, offb) : -INFINITY;
             const float mt = fmaxf(za, zb);
             float corr = 1.f;
             bool need_o = false;
@@ -585,28 +682,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
 
             // P = exp2(z - m_ref) as bf16, written over the chunk's S columns
-            float lsum = 0.f;
             uint32_t pk[CHUNK / 2];
-            {
-                const float ba = offa - mu;
-#pragma unroll
-                for (int c = 0; c < CHUNK; c += 2) {
-                    const float p0v = fast_exp2(fmaf(fa[c], sc, ba));
-                    const float p1v = fast_exp2(fmaf(fa[c + 1], sc, ba));
-                    lsum += p0v + p1v;
-                    pk[c / 2] = pack_bf16(p0v, p1v);
-                }
-                tmem_st16(tS, pk);
-            }
+            float lsum = chunk_exp(fa, cloa, ska, za, sc, offa, mu, pk);
+            tmem_st16(tS, pk);
             if (nch > 1) {
-                const float bbv = offb - mu;
-#pragma unroll
-                for (int c = 0; c < CHUNK; c += 2) {
-                    const float p0v = fast_exp2(fmaf(fb[c], sc, bbv));
-                    const float p1v = fast_exp2(fmaf(fb[c + 1], sc, bbv));
-                    lsum += p0v + p1v;
-                    pk[c / 2] = pack_bf16(p0v, p1v);
-                }
+                lsum += chunk_exp(fb, clob, skb, zb, sc, offb, mu, pk);
                 tmem_st16(tS + CHUNK / 2, pk);
             }
             l += lsum;
@@ -622,13 +702,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tc_fence_after();
                 const float f = need_o ? corr : 1.f;
 #pragma unroll
-                for (int oc = 0; oc < D / 32; ++oc) {
-                    uint32_t x[32];
-                    tmem_ld32(tbase + lane_base + O_COL + oc * 32, x);
+                for (int oc = 0; oc < D / 16; ++oc) {
+                    uint32_t x[16];
+                    tmem_ld16(tbase + lane_base + O_COL + oc * 16, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * f);
-                    tmem_st32(tbase + lane_base + O_COL + oc * 32, x);
+                    for (int c = 0; c < 16; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * f);
+                    tmem_st16(tbase + lane_base + O_COL + oc * 16, x);
                 }
             }
             tmem_wait_st();
@@ -649,19 +729,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_after();
             __syncwarp();
 #pragma unroll
-            for (int oc = 0; oc < D / 32; ++oc) {
-                uint32_t x[32];
-                tmem_ld32(tbase + lane_base + O_COL + oc * 32, x);
+            for (int oc = 0; oc < D / 16; ++oc) {  // 16 fp32 columns -> two 16-byte chunks
+                uint32_t x[16];
+                tmem_ld16(tbase + lane_base + O_COL + oc * 16, x);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[8];
 #pragma unroll
-                for (int c = 0; c < 32; c += 2)
+                for (int c = 0; c < 16; c += 2)
                     pk[c / 2] = pack_bf16(__uint_as_float(x[c]) * inv_l, __uint_as_float(x[c + 1]) * inv_l);
-                const int dc = oc >> 1, half = oc & 1;
+                const int dc = oc >> 2, quarter = oc & 3;
                 uint8_t *rowp = smem + C::Q_OFF + dc * C::Q_DBLK + r * ROW_BYTES;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int cidx = half * 4 + w;
+                for (int w = 0; w < 2; ++w) {
+                    const int cidx = quarter * 2 + w;
                     uint4 val = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
                     *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (r & 7)) << 4)) = val;
                 }
@@ -670,8 +750,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (ok && warp == 4 && lane == 0) {
+            const uint64_t stream_once = policy_evict_first();
             for (int dc = 0; dc < C::KD; ++dc)
-                tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0);
+                tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0, stream_once);
             tma_store_commit_and_wait();
         }
         if (ok && row_ok) {
