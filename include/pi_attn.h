@@ -212,6 +212,28 @@ int pi_attn_debug_probs(const void *q, const void *k, const void *v, const float
                         void *stream);
 
 /*
+ * pi_attn_debug_trace -- runs the bf16 tcgen05 forward (d = 64 or 128; writes out
+ * and lse as pi_attn_fwd does) and records, for CTAs 0 .. n_trace_ctas-1, the
+ * SM cycle counter (clock64) at the pipeline events of each CTA into
+ * trace [n_trace_ctas][232] int64 (caller-owned, zero-filled by the caller):
+ *   slot 0 entry, 1 set-up done, 2 Q load issued, 3 Q landed (seen by the S
+ *   issuer), 4 O complete (seen by the epilogue), 5 output stored, 6 exit,
+ *   7 number of key tiles; for tile t < 16: 8+t K load issued, 24+t V load
+ *   issued, 40+t S = QK^T issued, 56+t O += PV issued, 72+t S seen by the
+ *   softmax, 88+t P ready; and cycles spent in waits, each measured within
+ *   one thread: 104+t S issuer waiting for K, 120+t S issuer waiting for its
+ *   TMEM buffer, 136+t PV issuer waiting for P, 152+t PV issuer waiting for V,
+ *   168+t softmax waiting for S; softmax stamps inside tile t: 184+t S loaded
+ *   from TMEM, 200+t maxima done, 216+t P stored to TMEM.  Stamps of different
+ *   warps need not share a clock.  A profiling aid; the pages define no such
+ *   operation.
+ */
+int pi_attn_debug_trace(const void *q, const void *k, const void *v, const float *alpha,
+                        int B, int H, int Hkv, int N, int d, int k_local, int period, int S,
+                        int mode, void *out, float *lse, long long *trace, int n_trace_ctas,
+                        void *stream);
+
+/*
  * pi_attn_debug_wait_timeout -- launches one block that waits on a shared-memory
  * barrier nothing ever completes, giving up after timeout_us microseconds;
  * it then records PI_ERR_DEVICE_TIMEOUT in the status word and returns.

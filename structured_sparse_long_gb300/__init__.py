@@ -8,9 +8,10 @@ the first call loads the library and fails loudly if it is missing.
 """
 from ._binding import (MODE_ECP, MODE_PI, PiAttnError, bwd, bwd_noalloc,  # noqa: F401
                        bwd_workspace_size,
-                       debug_counts, debug_probs, debug_wait_timeout, fwd, lib_path, load,
+                       debug_counts, debug_probs, debug_trace, debug_wait_timeout, fwd, lib_path,
+                       load,
                        status, strerror)
 
 __all__ = ["fwd", "bwd", "bwd_noalloc", "bwd_workspace_size", "status", "strerror", "debug_counts",
-           "debug_probs", "debug_wait_timeout", "load", "lib_path", "PiAttnError",
+           "debug_probs", "debug_trace", "debug_wait_timeout", "load", "lib_path", "PiAttnError",
            "MODE_PI", "MODE_ECP"]

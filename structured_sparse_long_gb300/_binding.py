@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
         lib.pi_attn_debug_counts.argtypes = [P, P, P, P] + [I] * 10 + [P, P, P, P, P]
         lib.pi_attn_debug_probs.argtypes = [P, P, P, P, P] + [I] * 10 + [P, P, P, P]
         lib.pi_attn_debug_wait_timeout.argtypes = [I, P]
+        lib.pi_attn_debug_trace.argtypes = [P, P, P, P] + [I] * 9 + [P, P, P, I, P]
+        lib.pi_attn_debug_trace.restype = I
         for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
                      "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
                      "pi_attn_debug_wait_timeout"):
@@ -226,6 +228,19 @@ def debug_probs(q, k, v, alpha, lse_in, k_local, period, S, mode=MODE_PI, stream
                                     _ptr(lse), _ptr(P), _stream(stream))
     _check("pi_attn_debug_probs", rc)
     return P
+
+
+def debug_trace(q, k, v, alpha, k_local, period, S, mode=MODE_PI, n_ctas=256, stream=None):
+    """pi_attn_debug_trace. Returns (out, lse, trace int64 [n_ctas, 232]) of clock64 stamps."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    trace = torch.zeros((n_ctas, 232), device=q.device, dtype=torch.int64)
+    rc = load().pi_attn_debug_trace(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d,
+                                    k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(trace),
+                                    n_ctas, _stream(stream))
+    _check("pi_attn_debug_trace", rc)
+    return out, lse, trace
 
 
 def debug_wait_timeout(timeout_us: int, stream=None) -> None:

@@ -48,7 +48,17 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    """Compile and link the library.  Extra nvcc flags (e.g. -D tuning macros) can be given
+    in the PI_ATTN_NVCC_EXTRA environment variable; a change of them forces a rebuild."""
     nv = nvcc()
+    extra = os.environ.get("PI_ATTN_NVCC_EXTRA", "").split()
+    stamp = os.path.join(BUILD_DIR, "extra_flags.txt")
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    prev = open(stamp).read() if os.path.exists(stamp) else ""
+    if prev != " ".join(extra):
+        force = True
+        with open(stamp, "w") as fh:
+            fh.write(" ".join(extra))
     os.makedirs(BUILD_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "pi_attn.h")]
@@ -58,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         objs.append(o)
         if force or ptxas_info or _stale(o, [s] + headers):
-            cmd = [nv, "-c", s, "-o", o] + ARCH_FLAGS + NVCC_FLAGS
+            cmd = [nv, "-c", s, "-o", o] + ARCH_FLAGS + NVCC_FLAGS + extra
             if ptxas_info:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)

@@ -79,6 +79,7 @@ int run_fwd(const void *q, const void *k, const void *v, const float *alpha, int
     L.out = out; L.lse = lse;
     L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     L.fp32 = fp32; L.dbg = dbg; L.cnt = cnt; L.isum = isum; L.lse_in = lse_in; L.P = P;
+    L.trace = nullptr; L.n_trace = 0;
     L.status = status; L.timeout_ns = kWaitTimeoutNs;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!fp32 && d != 32) return map_cuda(pi::launch_fwd_tc(L, st));
@@ -234,6 +235,27 @@ int pi_attn_debug_probs(const void *q, const void *k, const void *v, const float
     if (!aligned(P, 4) || !aligned(lse_in, 4)) return PI_ERR_ALIGN;
     return run_fwd(q, k, v, alpha, B, H, Hkv, N, d, k_local, period, S, mode, out, lse, stream,
                    dtype == 1, 2, nullptr, nullptr, lse_in, P);
+}
+
+int pi_attn_debug_trace(const void *q, const void *k, const void *v, const float *alpha, int B, int H,
+                        int Hkv, int N, int d, int k_local, int period, int S, int mode, void *out,
+                        float *lse, long long *trace, int n_trace_ctas, void *stream) {
+    const int rc = validate_fwd(q, k, v, alpha, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
+    if (rc != PI_OK) return rc;
+    if (!trace) return PI_ERR_NULL;
+    if (d != 64 && d != 128) return PI_ERR_UNSUPPORTED;
+    if (n_trace_ctas < 0) return PI_ERR_SHAPE;
+    if (!aligned(trace, 8)) return PI_ERR_ALIGN;
+    int *status = status_word();
+    if (!status) return PI_ERR_CUDA;
+    pi::LaunchFwd L;
+    L.q = q; L.k = k; L.v = v; L.alpha = (mode == PI_MODE_PI) ? alpha : nullptr;
+    L.out = out; L.lse = lse;
+    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    L.fp32 = false; L.dbg = 3; L.cnt = nullptr; L.isum = nullptr; L.lse_in = nullptr; L.P = nullptr;
+    L.trace = trace; L.n_trace = n_trace_ctas;
+    L.status = status; L.timeout_ns = kWaitTimeoutNs;
+    return map_cuda(pi::launch_fwd_tc(L, static_cast<cudaStream_t>(stream)));
 }
 
 int pi_attn_debug_wait_timeout(int timeout_us, void *stream) {

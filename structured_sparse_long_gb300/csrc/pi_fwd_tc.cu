@@ -63,10 +63,13 @@ struct Cfg {
     static constexpr int B_VE = B_VF + STAGES;
     static constexpr int B_SF = B_VE + STAGES;
     static constexpr int B_PR = B_SF + 2;
+    // PV of tile U completes barrier B_PV + (U & 1), phase U >> 1: with two barriers no
+    // parity wait ever has two of its phases outstanding.
     static constexpr int B_PV = B_PR + 2;
-    static constexpr int B_OF = B_PV + 1;  // O complete (after the last PV), single phase
-    static constexpr int B_DR = B_OF + 1;
-    static constexpr int NBARS = B_DR + 1;
+    static constexpr int B_OF = B_PV + 2;  // O complete (after the last PV), single phase
+    static constexpr int B_DR = B_OF + 1;  // drain of the S issuer's MMAs
+    static constexpr int B_DR2 = B_DR + 1; // drain of the PV issuer's MMAs
+    static constexpr int NBARS = B_DR2 + 1;
     static constexpr int MISC_BYTES = NBARS * 8 + 16;
     static constexpr int SMEM_BYTES = BAR_OFF + MISC_BYTES + 1024;  // + alignment slack
 };
@@ -299,6 +302,25 @@ __device__ __forceinline__ float select32(const float *f, int x) {
     return (x & 16) ? d[1] : d[0];
 }
 
+// 2^x on the FMA pipe instead of the MUFU pipe: x = n + f with n = round(x) and f in
+// [-1/2, 1/2]; 2^f from a degree-3 polynomial (coefficients fitted by fit_exp2_poly.py next
+// to this file, max relative error 7.5e-5, far below the 2^-9 of the bf16 P it feeds) and
+// 2^n added into the exponent field.  Exactly 0 below 2^-126, like the masked logits need.
+__device__ __forceinline__ float exp2_poly(float x) {
+    const float xc = fmaxf(x, -126.f);
+    const float t = xc + 12582912.f;  // 1.5 * 2^23: the low bits of t now hold round(xc)
+    const float n = t - 12582912.f;
+    const float f = xc - n;
+    const float p = fmaf(fmaf(fmaf(0.0551716573536396f, f, 0.2426111400127411f), f,
+                              0.6932609677314758f), f, 0.9999280571937561f);
+    const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+    return (x < -126.f) ? 0.f : r;
+}
+
+#ifndef PI_EXP2_POLY_EVERY
+#define PI_EXP2_POLY_EVERY 0  // 0: every exp2 on MUFU; k > 0: one column pair in k on the FMA pipe
+#endif
+
 // Phase 1 of a key chunk for one row: mask the scores outside [clo, chi] and return the
 // chunk's largest logit in log2 units (prior included).  A skip chunk holds at most one
 // valid column per row (its diagonal), read with a select tree instead of a full pass.
@@ -307,13 +329,21 @@ __device__ __forceinline__ float chunk_max(float *f, int clo, int chi, bool skip
         if (clo > chi) return -INFINITY;
         return fmaf(select32(f, clo), sc, off);
     }
-    float mx = -INFINITY;
     if (!__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) f[c] = (c >= clo && c <= chi) ? f[c] : -INFINITY;
     }
+    // four independent partial maxima: a short dependency chain
+    float m0 = max3(f[0], f[1], f[2]), m1 = max3(f[3], f[4], f[5]);
+    float m2 = max3(f[6], f[7], f[8]), m3 = max3(f[9], f[10], f[11]);
 #pragma unroll
-    for (int c = 0; c < 32; c += 2) mx = max3(mx, f[c], f[c + 1]);
+    for (int c = 12; c < 32; c += 8) {
+        m0 = max3(m0, f[c], f[c + 1]);
+        m1 = max3(m1, f[c + 2], f[c + 3]);
+        m2 = max3(m2, f[c + 4], f[c + 5]);
+        m3 = max3(m3, f[c + 6], f[c + 7]);
+    }
+    const float mx = fmaxf(max3(m0, m1, m2), m3);
     return (mx == -INFINITY) ? -INFINITY : fmaf(mx, sc, off);
 }
 
@@ -333,19 +363,28 @@ __device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, f
     }
     const float bo = off - mu;
     const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo);
-    uint64_t acc = pack2(0.f, 0.f);
+    uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);  // two independent sums
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
         float z0, z1;
         unpack2(fma2(pack2(f[c], f[c + 1]), sc2, bo2), z0, z1);
-        const float p0 = fast_exp2(z0);
-        const float p1 = fast_exp2(z1);
-        acc = add2(acc, pack2(p0, p1));
+        float p0, p1;
+        if (PI_EXP2_POLY_EVERY > 0 && ((c >> 1) % (PI_EXP2_POLY_EVERY > 0 ? PI_EXP2_POLY_EVERY : 1)) ==
+                                          (PI_EXP2_POLY_EVERY > 0 ? PI_EXP2_POLY_EVERY - 1 : 0)) {
+            p0 = exp2_poly(z0);
+            p1 = exp2_poly(z1);
+        } else {
+            p0 = fast_exp2(z0);
+            p1 = fast_exp2(z1);
+        }
+        if ((c >> 1) & 1) acc1 = add2(acc1, pack2(p0, p1));
+        else acc0 = add2(acc0, pack2(p0, p1));
         pk[c / 2] = pack_bf16(p0, p1);
     }
-    float a0, a1;
-    unpack2(acc, a0, a1);
-    return a0 + a1;
+    float a0, a1, b0, b1;
+    unpack2(acc0, a0, a1);
+    unpack2(acc1, b0, b1);
+    return (a0 + a1) + (b0 + b1);
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
@@ -378,20 +417,33 @@ struct TcArgs {
     long long *isum;
     const float *lse_in;
     float *P;
+    long long *trace;  // DBG 3: clock64() stamps, kTraceSlots per traced CTA
+    int n_trace;       // DBG 3: CTAs 0 .. n_trace-1 are traced
 };
+
+// Trace layout (DBG 3), slots per CTA: 0 entry, 1 set-up done, 2 Q issued, 3 Q landed (MMA
+// side), 4 O complete (softmax side), 5 output stored, 6 exit, 7 tile count; then per tile t
+// (t < 16): 8+t K issued, 24+t V issued, 40+t S issued, 56+t PV issued, 72+t S seen by the
+// softmax, 88+t P ready; and cycles spent waiting, each measured within one thread:
+// 104+t S issuer on K, 120+t S issuer on the S buffer (PV of t-2), 136+t PV issuer on P,
+// 152+t PV issuer on V, 168+t softmax on S; softmax (warp 4) stamps inside tile t:
+// 184+t S loaded from TMEM, 200+t masked maxima done, 216+t P stored to TMEM (issued).
+// Absolute stamps of different warps need not share a clock; the waits are exact.
+constexpr int kTraceSlots = 232;
+constexpr int kTraceTiles = 16;
 
 // Key chunk ci of the block: first key position, whether it is a skip chunk,
 // its skip distance m*period and sub-block index u.
 struct ChunkWalk {
-    int lo0, n_band, m_first, cpb, p0, period;
+    int lo0, n_band, m_first, cpb, cpb_log2, p0, period;
     __device__ __forceinline__ int key0(int ci, int &back, int &u, bool &skip) const {
         if (ci < n_band) {
             back = 0; u = 0; skip = false;
             return lo0 + ci * CHUNK;
         }
-        const int sc = ci - n_band;
-        const int m = m_first + sc / cpb;
-        u = sc % cpb;
+        const int sc = ci - n_band;  // cpb = R / 32 is 1, 2 or 4
+        const int m = m_first + (sc >> cpb_log2);
+        u = sc & (cpb - 1);
         back = m * period;
         skip = true;
         return p0 - back + u * CHUNK;
@@ -420,6 +472,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const Shape &s = args.s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtx wc{abort_flag, args.status, args.timeout_ns};
+    auto stamp = [&](int slot) {
+        if (DBG == 3 && (int)blockIdx.x < args.n_trace)
+            args.trace[(long long)blockIdx.x * kTraceSlots + slot] = (long long)clock64();
+    };
+    auto stamp_tile = [&](int base, int t) {
+        if (t < kTraceTiles) stamp(base + t);
+    };
+    // bounded wait that also records how long it took (DBG 3)
+    auto timed_wait = [&](uint32_t b, uint32_t parity, int slot_base, int t) -> bool {
+        const long long c0 = (DBG == 3) ? (long long)clock64() : 0;
+        const bool r = wait_bar(b, parity, wc);
+        if (DBG == 3 && t < kTraceTiles && (int)blockIdx.x < args.n_trace)
+            args.trace[(long long)blockIdx.x * kTraceSlots + slot_base + t] = (long long)clock64() - c0;
+        return r;
+    };
+    if (threadIdx.x == 0) stamp(0);
 
     // ---- block coordinates: (b, head group, position block), positions fastest
     const int GP = args.GP;
@@ -440,6 +508,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     cw.p0 = p0;
     cw.period = s.period;
     cw.cpb = R / CHUNK;
+    cw.cpb_log2 = (cw.cpb == 4) ? 2 : (cw.cpb == 2) ? 1 : 0;
     cw.lo0 = band_lo(p0, s.mode, s.k_local);
     const int band_hi = min(s.N - 1, p0 + R - 1);
     cw.n_band = (band_hi - cw.lo0) / CHUNK + 1;
@@ -467,8 +536,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(bar(C::B_PR + i), 128);
         }
         mbar_init(bar(C::B_PV), 1);
+        mbar_init(bar(C::B_PV + 1), 1);
         mbar_init(bar(C::B_OF), 1);
         mbar_init(bar(C::B_DR), 1);
+        mbar_init(bar(C::B_DR2), 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -477,6 +548,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    if (threadIdx.x == 0) {
+        stamp(1);
+        if (DBG == 3 && (int)blockIdx.x < args.n_trace)
+            args.trace[(long long)blockIdx.x * kTraceSlots + 7] = n_tiles;
+    }
 
     if (warp == 0) {
         // ================= producer: Q and K tiles
@@ -488,11 +564,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int dc = 0; dc < C::KD; ++dc)
                 tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
                                  stream_once);
+            stamp(2);
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
                 const int nch = min(2, n_chunks - 2 * t);
+                stamp_tile(8, t);
                 mbar_expect_tx(bar(C::B_KF + st), nch * C::KD * BOX_BYTES);
                 for (int cc = 0; cc < nch; ++cc) {
                     int back, u;
@@ -522,6 +600,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
                 const int nch = min(2, n_chunks - 2 * t);
+                stamp_tile(24, t);
                 mbar_expect_tx(bar(C::B_VF + st), nch * C::KD * BOX_BYTES);
                 for (int cc = 0; cc < nch; ++cc) {
                     int back, u;
@@ -541,54 +620,66 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         }
     } else if (warp == 1) {
-        // ================= MMA issuer
+        // ================= S issuer: S = Q K^T into the tile's TMEM buffer.  It runs ahead of
+        // the PV issuer, so that a PV never waits behind a K tile still in flight.
         if (lane == 0) {
             bool ok = wait_bar(bar(C::B_Q), 0, wc);
-            for (int t = 0; ok && t <= n_tiles; ++t) {
-                if (t < n_tiles) {
-                    const int st = t % ST, buf = t & 1;
-                    if (!wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc)) break;
-                    if (t >= 2 && !wait_bar(bar(C::B_PV), (t - 2) & 1, wc)) break;
-                    tc_fence_after();
-                    const int nch = min(2, n_chunks - 2 * t);
-                    const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
-                    const uint32_t dS = tbase + buf * TILE_N;
+            if (ok) stamp(3);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int st = t % ST, buf = t & 1;
+                if (!timed_wait(bar(C::B_KF + st), (t / ST) & 1, 104, t)) break;
+                // buffer buf last held P of tile t-2: its PV must be done
+                if (t >= 2 && !timed_wait(bar(C::B_PV + buf), ((t - 2) >> 1) & 1, 120, t)) break;
+                tc_fence_after();
+                const int nch = min(2, n_chunks - 2 * t);
+                const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
+                const uint32_t dS = tbase + buf * TILE_N;
 #pragma unroll
-                    for (int dc = 0; dc < C::KD; ++dc) {
+                for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t a = sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024);
-                            const uint64_t bb =
-                                sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024);
-                            mma_ss(dS, a, bb, idesc, (dc | ks) != 0);
-                        }
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t a = sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024);
+                        const uint64_t bb =
+                            sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024);
+                        mma_ss(dS, a, bb, idesc, (dc | ks) != 0);
                     }
-                    tc_commit(bar(C::B_SF + buf));
-                    tc_commit(bar(C::B_KE + st));
                 }
-                if (t >= 1) {
-                    const int u = t - 1, st = u % ST, buf = u & 1;
-                    if (!wait_bar(bar(C::B_PR + buf), (u >> 1) & 1, wc)) break;
-                    if (!wait_bar(bar(C::B_VF + st), (u / ST) & 1, wc)) break;
-                    tc_fence_after();
-                    const int nch = min(2, n_chunks - 2 * u);
-                    const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
-                    const uint32_t aP = tbase + buf * TILE_N;
-                    for (int kk = 0; kk < 2 * nch; ++kk) {
-                        const uint64_t bb = sdesc(sV + st * C::KV_STAGE + kk * 16 * ROW_BYTES,
-                                                  C::KV_DBLK, 1024);
-                        mma_ts(tbase + O_COL, aP + kk * 8, bb, idesc, (u > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(bar(C::B_PV));
-                    tc_commit(bar(C::B_VE + st));
-                    if (u == n_tiles - 1) tc_commit(bar(C::B_OF));
-                }
+                stamp_tile(40, t);
+                tc_commit(bar(C::B_SF + buf));
+                tc_commit(bar(C::B_KE + st));
             }
-            // every MMA issued so far has finished before TMEM is released
+            // every MMA this thread issued has finished before TMEM is released
             tc_commit(bar(C::B_DR));
             volatile uint32_t zero = 0;
             WaitCtx w2{&zero, args.status, args.timeout_ns};
             wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp == 3) {
+        // ================= PV issuer: O += P V with P read from TMEM
+        if (lane == 0) {
+            bool ok = true;
+            for (int u = 0; ok && u < n_tiles; ++u) {
+                const int st = u % ST, buf = u & 1;
+                if (!timed_wait(bar(C::B_PR + buf), (u >> 1) & 1, 136, u)) break;
+                if (!timed_wait(bar(C::B_VF + st), (u / ST) & 1, 152, u)) break;
+                tc_fence_after();
+                const int nch = min(2, n_chunks - 2 * u);
+                const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
+                const uint32_t aP = tbase + buf * TILE_N;
+                for (int kk = 0; kk < 2 * nch; ++kk) {
+                    const uint64_t bb = sdesc(sV + st * C::KV_STAGE + kk * 16 * ROW_BYTES,
+                                              C::KV_DBLK, 1024);
+                    mma_ts(tbase + O_COL, aP + kk * 8, bb, idesc, (u > 0 || kk > 0) ? 1u : 0u);
+                }
+                stamp_tile(56, u);
+                tc_commit(bar(C::B_PV + buf));
+                tc_commit(bar(C::B_VE + st));
+                if (u == n_tiles - 1) tc_commit(bar(C::B_OF));
+            }
+            tc_commit(bar(C::B_DR2));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR2), 0, w2);
         }
     } else if (warp >= 4) {
         // ================= softmax + epilogue: one thread per row
@@ -631,9 +722,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
         for (int t = 0; t < n_tiles; ++t) {
             const int buf = t & 1;
-            ok = wait_bar(bar(C::B_SF + buf), (t >> 1) & 1, wc);
+            if (warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (t >> 1) & 1, 168, t);
+            else ok = wait_bar(bar(C::B_SF + buf), (t >> 1) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            if (warp == 4 && lane == 0) stamp_tile(72, t);
             tc_fence_after();
             __syncwarp();
             const int nch = min(2, n_chunks - 2 * t);
@@ -642,6 +735,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tmem_ld32(tS, ra);
             if (nch > 1) tmem_ld32(tS + CHUNK, rb);
             tmem_wait_ld();
+            if (warp == 4 && lane == 0) stamp_tile(184, t);
 
             int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
             float offa, offb = 0.f;
@@ -654,6 +748,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const float za = chunk_max(fa, cloa, chia, ska, sc, offa);
             const float zb = (nch > 1) ? chunk_max(fb, clob, chib, skb, sc, offb) : -INFINITY;
             const float mt = fmaxf(za, zb);
+            if (warp == 4 && lane == 0) stamp_tile(200, t);
             float corr = 1.f;
             bool need_o = false;
             if (mt > m_ref + kRescaleThreshold) {
@@ -689,14 +784,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 lsum += chunk_exp(fb, clob, skb, zb, sc, offb, mu, pk);
                 tmem_st16(tS + CHUNK / 2, pk);
             }
+            if (warp == 4 && lane == 0) stamp_tile(216, t);
             l += lsum;
             __syncwarp();
 
             // Rescale this row of O when the reference max moved.  PV of tile t-1 must be done.
-            // The wait names that phase exactly: S of tile t implies PV of tile t-2 finished,
-            // and PV of tile t cannot start before this thread arrives below.
+            // The wait names that phase exactly: S of tile t-1 implied PV of tile t-3 finished,
+            // and PV of tile t+1 cannot start before this thread arrives for tile t+1.
             if (__any_sync(0xffffffffu, need_o)) {
-                ok = wait_bar(bar(C::B_PV), (t - 1) & 1, wc);
+                ok = wait_bar(bar(C::B_PV + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -714,6 +810,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_PR + buf));
+            if (warp == 4 && lane == 0) stamp_tile(88, t);
         }
 
         // ---- epilogue: O / l -> bf16 -> shared (swizzled, reusing the Q buffer) -> TMA store
@@ -724,6 +821,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             ok = wait_bar(bar(C::B_OF), 0, wc);
             ok = __all_sync(0xffffffffu, ok);
         }
+        if (warp == 4 && lane == 0) stamp(4);
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         if (ok) {
             tc_fence_after();
@@ -754,6 +852,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int dc = 0; dc < C::KD; ++dc)
                 tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0, stream_once);
             tma_store_commit_and_wait();
+            stamp(5);
         }
         if (ok && row_ok) {
             args.lse[row_g] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
@@ -767,6 +866,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ---- teardown
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) stamp(6);
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
@@ -859,17 +959,20 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
-    TcArgs a{L.alpha, L.lse, s, GP, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P};
+    TcArgs a{L.alpha, L.lse, s, GP, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P,
+             L.trace, L.n_trace};
     const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (s.d == 64) {
         if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
         if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 3) return launch<64, 3>(mq, mk, mv, mo, a, (unsigned)grid, st);
         return launch<64, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
     }
     if (s.d == 128) {
         if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
         if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 3) return launch<128, 3>(mq, mk, mv, mo, a, (unsigned)grid, st);
         return launch<128, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
     }
     return cudaErrorInvalidValue;

@@ -15,11 +15,13 @@ struct LaunchFwd {
     float *lse;
     Shape s;
     bool fp32;
-    int dbg;               // 0 forward, 1 + counts, 2 + probability dump
+    int dbg;               // 0 forward, 1 + counts, 2 + probability dump, 3 + timeline trace
     int *cnt;              // dbg 1
     long long *isum;       // dbg 1
     const float *lse_in;   // dbg 2
     float *P;              // dbg 2
+    long long *trace;      // dbg 3: per-CTA clock64() stamps (tcgen05 kernel)
+    int n_trace;           // dbg 3: number of traced CTAs
     int *status;           // device status word
     uint64_t timeout_ns;   // bound on every device-side wait
 };

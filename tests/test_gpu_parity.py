@@ -249,3 +249,24 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert pa.status() == -7
     assert pa.status() == 0  # reading clears it
     check_forward(WORKLOADS["C1"])  # the context is still usable
+
+
+def test_trace_mode_matches_forward_and_stamps_are_ordered():
+    """pi_attn_debug_trace runs the same forward: identical out/lse, and per-tile stamps of
+    the softmax warp (one clock) are in order."""
+    w = WORKLOADS["C2"]
+    inp, dev, out, lse = run_forward(w)
+    out2, lse2, tr = pa.debug_trace(dev["q"], dev["k"], dev["v"], dev["alpha"], w.k_local, w.period,
+                                    w.S, w.mode, n_ctas=64)
+    torch.cuda.synchronize()
+    assert pa.status() == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    T = tr.cpu().numpy()
+    for c in range(64):
+        nt = int(T[c, 7])
+        assert 1 <= nt <= 16
+        for t in range(nt):
+            seen, loaded, maxed, stored, ready = (T[c, 72 + t], T[c, 184 + t], T[c, 200 + t],
+                                                  T[c, 216 + t], T[c, 88 + t])
+            assert 0 < seen <= loaded <= maxed <= stored <= ready
+            assert T[c, 168 + t] >= 0 and T[c, 104 + t] >= 0
