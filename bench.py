@@ -88,7 +88,7 @@ def load_peaks():
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for name in ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h"):
+    for name in ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"):
         with open(os.path.join(ROOT, "structured_sparse_long_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

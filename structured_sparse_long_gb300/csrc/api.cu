@@ -108,7 +108,15 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
     L.Dws = static_cast<float *>(workspace);
     L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     L.fp32 = fp32;
-    return map_cuda(pi::launch_bwd_simt(L, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!fp32 && d != 32) {
+        int *status = status_word();
+        if (!status) return PI_ERR_CUDA;
+        const cudaError_t e = pi::launch_bwd_dq_tc(L, status, kWaitTimeoutNs, st);
+        if (e != cudaSuccess) return PI_ERR_CUDA;
+        return map_cuda(pi::launch_bwd_dkdv_simt(L, st));
+    }
+    return map_cuda(pi::launch_bwd_simt(L, st));
 }
 
 }  // namespace

@@ -1,0 +1,883 @@
+// pi_bwd_tc.cu -- backward of the fused pi-Attention / ECP attention on sm_103a tensor cores.
+//
+// The chain rule through the forward's definition ("pi-Attention: Periodic Sparse
+// Transformers for Efficient Long-Context Modeling", section 2.1-2.3; ECP page section 2):
+//   p_ij = exp(z_ij - lse_i),  dp_ij = dout_i . v_j,  D_i = sum_j p_ij dp_ij,
+//   dz_ij = p_ij (dp_ij - D_i),
+//   dq_i = tau sum_j dz_ij k_j = tau (sum_j (p dp)_ij k_j - D_i sum_j p_ij k_j),
+//   dk_j = tau sum_{h in group, i} dz_ij q_i,  dv_j = sum_{h in group, i} p_ij dout_i,
+//   dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)).
+//
+// Kernel 1 (query-major, one CTA per 128 query rows laid out as in the forward):
+//   per key tile, S = Q K^T and dP = dO V^T into TMEM; one thread per row forms p and p*dp,
+//   keeps D_i and the skip sums of dalpha in registers and writes p and p*dp (bf16) back to
+//   TMEM; two MMAs accumulate A1 = sum (p dp) K and A2 = sum p K.  The epilogue writes
+//   dq = tau (A1 - D A2), D_i (for kernel 2) and dalpha.  One sweep over the keys, and D_i
+//   is exact: it never goes through the bf16-rounded out.
+// Kernel 2 (key-major, one CTA per 128 keys of a KV head): for every 64-query chunk of every
+//   query head of the group whose band contains these keys, and every chunk of skip queries
+//   j + m*period: S^T = K Q^T and dP^T = V dO^T into TMEM; one thread per key forms p and dz
+//   with the chunk's per-query bias (prior - lse) and D, writes them (bf16) back to TMEM; two
+//   MMAs accumulate dV += P^T dO and dK += dZ^T Q.  No atomics: deterministic.
+#include <algorithm>
+
+#include "pi_common.cuh"
+#include "pi_launch.h"
+#include "pi_tc_ptx.cuh"
+
+namespace pi {
+namespace tcb {
+
+using namespace tc;
+
+constexpr int BM = 128;     // rows per CTA (MMA M)
+constexpr int CHUNK = 32;   // keys per chunk (TMA box rows)
+constexpr int TILE_N = 64;  // keys per tile
+constexpr int NUM_THREADS = 256;
+constexpr int ROW_BYTES = 128;
+constexpr int BOX_BYTES = CHUNK * ROW_BYTES;
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+
+// Key chunk walk of a q-block: identical enumeration to the forward kernel's.
+struct QWalk {
+    int lo0, n_band, m_first, cpb, cpb_log2, p0, period;
+    __device__ __forceinline__ int key0(int ci, int &back, bool &skip) const {
+        if (ci < n_band) {
+            back = 0;
+            skip = false;
+            return lo0 + ci * CHUNK;
+        }
+        const int sc = ci - n_band;
+        const int m = m_first + (sc >> cpb_log2);
+        const int u = sc & (cpb - 1);
+        back = m * period;
+        skip = true;
+        return p0 - back + u * CHUNK;
+    }
+};
+
+template <int D>
+struct CfgQ {
+    static constexpr int KD = D / 64;
+    static constexpr int ST = (D == 64) ? 4 : 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int Q_DBLK = BM * ROW_BYTES;
+    static constexpr int KV_STAGE = TILE_N * D * 2;
+    static constexpr int KV_DBLK = TILE_N * ROW_BYTES;
+    static constexpr int Q_OFF = 0;
+    static constexpr int G_OFF = Q_BYTES;  // dO tile
+    static constexpr int K_OFF = 2 * Q_BYTES;
+    static constexpr int V_OFF = K_OFF + ST * KV_STAGE;
+    static constexpr int BAR_OFF = V_OFF + ST * KV_STAGE;
+    static constexpr int B_QF = 0;
+    static constexpr int B_KF = 1;
+    static constexpr int B_KE = B_KF + ST;
+    static constexpr int B_VF = B_KE + ST;
+    static constexpr int B_VE = B_VF + ST;
+    static constexpr int B_SF = B_VE + ST;  // S and dP of the tile in TMEM
+    static constexpr int B_PR = B_SF + 1;   // p and p*dp written back (128 arrivals)
+    static constexpr int B_BF = B_PR + 1;   // A1/A2 MMAs of the tile done: S/dP columns free
+    static constexpr int B_AF = B_BF + 1;   // A1/A2 complete (single phase)
+    static constexpr int B_DR = B_AF + 1;
+    static constexpr int NBARS = B_DR + 1;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    // TMEM columns
+    static constexpr int S_COL = 0, DP_COL = 64, A1_COL = 128, A2_COL = 128 + D;
+    static constexpr int TMEM_COLS = (A2_COL + D <= 256) ? 256 : 512;
+};
+
+struct DqArgs {
+    const float *alpha;
+    const float *lse;
+    float *Dws;
+    float *dalpha;
+    Shape s;
+    int GP;
+    int *status;
+    uint64_t timeout_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmDQ, const DqArgs args) {
+    using C = CfgQ<D>;
+    constexpr int ST = C::ST;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const uint32_t sQ = sbase + C::Q_OFF, sG = sbase + C::G_OFF, sK = sbase + C::K_OFF,
+                   sV = sbase + C::V_OFF, sBar = sbase + C::BAR_OFF;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NBARS * 8);
+    uint32_t *tmem_slot = misc;
+    volatile uint32_t *abort_flag = misc + 1;
+    auto bar = [&](int idx) -> uint32_t { return sBar + idx * 8; };
+
+    const Shape &s = args.s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtx wc{abort_flag, args.status, args.timeout_ns};
+
+    // ---- q-block coordinates and key chunks (as in the forward)
+    const int GP = args.GP;
+    const int R = BM / GP;
+    const int nqb = (s.N + R - 1) / R;
+    const int hsub = s.H / GP;
+    int bid = blockIdx.x;
+    const int pb = bid % nqb;
+    bid /= nqb;
+    const int hs = bid % hsub;
+    const int b = bid / hsub;
+    const int h0 = hs * GP;
+    const int g = h0 / (s.H / s.Hkv);
+    const int p0 = pb * R;
+    QWalk cw;
+    cw.p0 = p0;
+    cw.period = s.period;
+    cw.cpb = R / CHUNK;
+    cw.cpb_log2 = (cw.cpb == 4) ? 2 : (cw.cpb == 2) ? 1 : 0;
+    cw.lo0 = band_lo(p0, s.mode, s.k_local);
+    cw.n_band = (min(s.N - 1, p0 + R - 1) - cw.lo0) / CHUNK + 1;
+    int n_skip_blocks = 0;
+    cw.m_first = 1;
+    if (s.mode == 0 && s.S > 0) {
+        cw.m_first = max(1, s.k_local / s.period + 1);
+        const int m_last = min(s.S, (p0 + R - 1) / s.period);
+        n_skip_blocks = max(0, m_last - cw.m_first + 1);
+    }
+    const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
+    const int n_tiles = (n_chunks + 1) / 2;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QF), 1);
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(bar(C::B_KF + i), 1);
+            mbar_init(bar(C::B_KE + i), 1);
+            mbar_init(bar(C::B_VF + i), 1);
+            mbar_init(bar(C::B_VE + i), 1);
+        }
+        mbar_init(bar(C::B_SF), 1);
+        mbar_init(bar(C::B_PR), 128);
+        mbar_init(bar(C::B_BF), 1);
+        mbar_init(bar(C::B_AF), 1);
+        mbar_init(bar(C::B_DR), 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= producer: Q, dO, K tiles
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmG);
+            prefetch_tmap(&tmK);
+            const uint64_t once = policy_evict_first(), reused = policy_evict_last();
+            mbar_expect_tx(bar(C::B_QF), 2 * C::Q_BYTES);
+            for (int dc = 0; dc < C::KD; ++dc) {
+                tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_QF), once);
+                tma_load_3d_hint(sG + dc * C::Q_DBLK, &tmG, dc * 64, p0, b * s.H + h0, bar(C::B_QF), once);
+            }
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % ST, round = t / ST;
+                if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
+                const int nch = min(2, n_chunks - 2 * t);
+                mbar_expect_tx(bar(C::B_KF + st), nch * C::KD * BOX_BYTES);
+                for (int cc = 0; cc < nch; ++cc) {
+                    int back;
+                    bool sk;
+                    const int key0 = cw.key0(2 * t + cc, back, sk);
+                    for (int dc = 0; dc < C::KD; ++dc)
+                        tma_load_3d_hint(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
+                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st), reused);
+                }
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                volatile uint32_t zero = 0;
+                WaitCtx w2{&zero, nullptr, 20000000ull};
+                wait_bar(bar(C::B_QF), 0, w2);
+                for (int t = max(0, issued - ST); t < issued; ++t)
+                    wait_bar(bar(C::B_KF + t % ST), (t / ST) & 1, w2);
+            }
+        }
+    } else if (warp == 2) {
+        // ================= producer: V tiles
+        if (lane == 0) {
+            prefetch_tmap(&tmV);
+            const uint64_t reused = policy_evict_last();
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % ST, round = t / ST;
+                if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
+                const int nch = min(2, n_chunks - 2 * t);
+                mbar_expect_tx(bar(C::B_VF + st), nch * C::KD * BOX_BYTES);
+                for (int cc = 0; cc < nch; ++cc) {
+                    int back;
+                    bool sk;
+                    const int key0 = cw.key0(2 * t + cc, back, sk);
+                    for (int dc = 0; dc < C::KD; ++dc)
+                        tma_load_3d_hint(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
+                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st), reused);
+                }
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                volatile uint32_t zero = 0;
+                WaitCtx w2{&zero, nullptr, 20000000ull};
+                for (int t = max(0, issued - ST); t < issued; ++t)
+                    wait_bar(bar(C::B_VF + t % ST), (t / ST) & 1, w2);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0) {
+            bool ok = wait_bar(bar(C::B_QF), 0, wc);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int st = t % ST;
+                if (!wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc)) break;
+                if (!wait_bar(bar(C::B_VF + st), (t / ST) & 1, wc)) break;
+                // the S/dP columns still hold the operands of tile t-1's A1/A2 MMAs
+                if (t >= 1 && !wait_bar(bar(C::B_BF), (t - 1) & 1, wc)) break;
+                tc_fence_after();
+                const int nch = min(2, n_chunks - 2 * t);
+                const uint32_t idesc_s = idesc_bf16(BM, CHUNK * nch, 0, 0);
+#pragma unroll
+                for (int dc = 0; dc < C::KD; ++dc) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc = (dc | ks) != 0;
+                        mma_ss(tbase + C::S_COL, sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024),
+                               sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
+                               idesc_s, acc);
+                        mma_ss(tbase + C::DP_COL, sdesc(sG + dc * C::Q_DBLK + ks * 32, 16, 1024),
+                               sdesc(sV + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
+                               idesc_s, acc);
+                    }
+                }
+                tc_commit(bar(C::B_SF));
+                tc_commit(bar(C::B_VE + st));
+                if (!wait_bar(bar(C::B_PR), t & 1, wc)) break;
+                tc_fence_after();
+                const uint32_t idesc_a = idesc_bf16(BM, D, 0, 1);
+                for (int kk = 0; kk < 2 * nch; ++kk) {
+                    const uint64_t kb = sdesc(sK + st * C::KV_STAGE + kk * 16 * ROW_BYTES, C::KV_DBLK, 1024);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tbase + C::A1_COL, tbase + C::S_COL + kk * 8, kb, idesc_a, acc);
+                    mma_ts(tbase + C::A2_COL, tbase + C::DP_COL + kk * 8, kb, idesc_a, acc);
+                }
+                tc_commit(bar(C::B_BF));
+                tc_commit(bar(C::B_KE + st));
+                if (t == n_tiles - 1) tc_commit(bar(C::B_AF));
+            }
+            tc_commit(bar(C::B_DR));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp >= 4) {
+        // ================= one thread per query row
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const int hh = r / R, trow = r % R;
+        const int i = p0 + trow;
+        const int h = h0 + hh;
+        const bool row_ok = i < s.N;
+        const long long row_g = ((long long)b * s.H + h) * s.N + i;
+        const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
+        const float off_band = (s.mode == 0) ? log2f(al) : 0.f;
+        const float off_skip = log2f(1.f - al);
+        const float lse2 = row_ok ? args.lse[row_g] * kLog2e : -INFINITY;
+        const bool live = row_ok && lse2 != -INFINITY;
+        const int lo_i = band_lo(i, s.mode, s.k_local);
+        const float sc = s.scale_log2;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        float dsum = 0.f, skip_p = 0.f, skip_pdp = 0.f;
+        bool any_skip = false;
+        bool ok = true;
+
+        for (int t = 0; t < n_tiles; ++t) {
+            ok = wait_bar(bar(C::B_SF), t & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            const int nch = min(2, n_chunks - 2 * t);
+            for (int cc = 0; cc < nch; ++cc) {
+                int back;
+                bool sk;
+                const int key0 = cw.key0(2 * t + cc, back, sk);
+                int clo, chi;
+                float off;
+                if (!sk) {
+                    clo = max(lo_i - key0, 0);
+                    chi = min(i - key0, CHUNK - 1);
+                    off = off_band;
+                } else {
+                    const int jk = i - back, c = jk - key0;
+                    if (jk >= 0 && c >= 0 && c < CHUNK) { clo = c; chi = c; }
+                    else { clo = CHUNK; chi = -1; }
+                    off = off_skip;
+                    any_skip |= (clo <= chi);
+                }
+                if (!live) { clo = CHUNK; chi = -1; }
+                const float bo = off - lse2;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[16], dr[16];
+                    tmem_ld16(tbase + lane_base + C::S_COL + cc * CHUNK + half * 16, sr);
+                    tmem_ld16(tbase + lane_base + C::DP_COL + cc * CHUNK + half * 16, dr);
+                    tmem_wait_ld();
+                    uint32_t pw[8], pp[8];
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        const int c0 = half * 16 + c;
+                        const bool v0 = c0 >= clo && c0 <= chi, v1 = c0 + 1 >= clo && c0 + 1 <= chi;
+                        const float p0v = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), sc, bo)) : 0.f;
+                        const float p1v = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, bo)) : 0.f;
+                        const float w0 = p0v * __uint_as_float(dr[c]);
+                        const float w1 = p1v * __uint_as_float(dr[c + 1]);
+                        dsum += w0 + w1;
+                        if (sk) {
+                            skip_p += p0v + p1v;
+                            skip_pdp += w0 + w1;
+                        }
+                        pp[c / 2] = pack_bf16(p0v, p1v);
+                        pw[c / 2] = pack_bf16(w0, w1);
+                    }
+                    // A1 operand (p*dp) over the S columns, A2 operand (p) over the dP columns;
+                    // both chunk halves' values are already in registers
+                    tmem_st8(tbase + lane_base + C::S_COL + cc * (CHUNK / 2) + half * 8, pw);
+                    tmem_st8(tbase + lane_base + C::DP_COL + cc * (CHUNK / 2) + half * 8, pp);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PR));
+        }
+
+        // ---- epilogue: dq = tau (A1 - D A2) -> bf16 -> shared (Q buffer) -> TMA store
+        if (ok) {
+            ok = wait_bar(bar(C::B_AF), 0, wc);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        const float tau = s.scale_log2 / kLog2e;
+        if (ok) {
+            tc_fence_after();
+            __syncwarp();
+#pragma unroll
+            for (int oc = 0; oc < D / 16; ++oc) {
+                uint32_t a1[16], a2[16];
+                tmem_ld16(tbase + lane_base + C::A1_COL + oc * 16, a1);
+                tmem_ld16(tbase + lane_base + C::A2_COL + oc * 16, a2);
+                tmem_wait_ld();
+                uint32_t pk[8];
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const float x0 = tau * (__uint_as_float(a1[c]) - dsum * __uint_as_float(a2[c]));
+                    const float x1 = tau * (__uint_as_float(a1[c + 1]) - dsum * __uint_as_float(a2[c + 1]));
+                    pk[c / 2] = pack_bf16(x0, x1);
+                }
+                const int dc = oc >> 2, quarter = oc & 3;
+                uint8_t *rowp = smem + C::Q_OFF + dc * C::Q_DBLK + r * ROW_BYTES;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int cidx = quarter * 2 + w;
+                    *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (ok && warp == 4 && lane == 0) {
+            const uint64_t once = policy_evict_first();
+            for (int dc = 0; dc < C::KD; ++dc)
+                tma_store_3d(&tmDQ, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0, once);
+            tma_store_commit_and_wait();
+        }
+        if (ok && row_ok) {
+            args.Dws[row_g] = dsum;
+            if (args.dalpha) {
+                any_skip = any_skip && live;
+                args.dalpha[row_g] =
+                    (s.mode == 0 && any_skip) ? -(skip_pdp - dsum * skip_p) / (al * (1.f - al)) : 0.f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+static cudaError_t launch_dq(const CUtensorMap &mq, const CUtensorMap &mg, const CUtensorMap &mk,
+                            const CUtensorMap &mv, const CUtensorMap &mdq, const DqArgs &a,
+                            unsigned grid, cudaStream_t st) {
+    constexpr int smem = CfgQ<D>::SMEM_BYTES;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    bwd_dq_tc_kernel<D><<<grid, NUM_THREADS, smem, st>>>(mq, mg, mk, mv, mdq, a);
+    return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------- kernel 2
+
+constexpr int QC = 64;      // queries per chunk (N of the transposed MMAs)
+constexpr int BK = 128;     // keys per CTA (M)
+
+// The query chunks that attend to keys [j0, j0 + 128) of one KV head, for one query head:
+// band chunks i0 = j0 + 64c up to the last query whose band holds key j0 + 127, then two
+// chunks per skip multiple m (queries j0 + m*period + [0, 128)).
+struct KWalk {
+    int j0, n_band, m_first, n_skip, period, per_head;
+    __device__ __forceinline__ void chunk(int ci, int &hh, int &i0, int &back, bool &skip) const {
+        hh = ci / per_head;
+        const int c = ci - hh * per_head;
+        if (c < n_band) {
+            i0 = j0 + c * QC;
+            back = 0;
+            skip = false;
+        } else {
+            const int sc = c - n_band;
+            const int m = m_first + (sc >> 1);
+            back = m * period;
+            i0 = j0 + back + (sc & 1) * QC;
+            skip = true;
+        }
+    }
+};
+
+template <int D>
+struct CfgK {
+    static constexpr int KD = D / 64;
+    static constexpr int ST = 3;  // query-chunk stages
+    static constexpr int KT_BYTES = BK * D * 2;
+    static constexpr int KT_DBLK = BK * ROW_BYTES;
+    static constexpr int QC_BYTES = QC * D * 2;
+    static constexpr int QC_DBLK = QC * ROW_BYTES;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = KT_BYTES;
+    static constexpr int Q_OFF = 2 * KT_BYTES;                // [ST] Q chunks
+    static constexpr int G_OFF = Q_OFF + ST * QC_BYTES;        // [ST] dO chunks
+    static constexpr int X_OFF = G_OFF + ST * QC_BYTES;        // [ST][2][QC] fp32: bias, D
+    static constexpr int BAR_OFF = X_OFF + ST * 2 * QC * 4;
+    static constexpr int B_KV = 0;                 // K and V tiles landed
+    static constexpr int B_QF = 1;                 // [ST] Q/dO chunk landed
+    static constexpr int B_QE = B_QF + ST;         // [ST] chunk consumed by its dV/dK MMAs
+    static constexpr int B_XF = B_QE + ST;         // [ST] per-query vectors ready (32 arrivals)
+    static constexpr int B_XE = B_XF + ST;         // [ST] vectors consumed (128 arrivals)
+    static constexpr int B_SF = B_XE + ST;         // S^T, dP^T in TMEM
+    static constexpr int B_PR = B_SF + 1;          // P^T, dZ^T written back (128 arrivals)
+    static constexpr int B_BF = B_PR + 1;          // dV/dK MMAs of the chunk done
+    static constexpr int B_OF = B_BF + 1;          // dK, dV complete (single phase)
+    static constexpr int B_DR = B_OF + 1;
+    static constexpr int NBARS = B_DR + 1;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static constexpr int ST_COL = 0, DPT_COL = 64, DV_COL = 128, DK_COL = 128 + D;
+    static constexpr int TMEM_COLS = (DK_COL + D <= 256) ? 256 : 512;
+};
+
+struct DkvArgs {
+    const float *alpha;
+    const float *lse;
+    const float *Dws;
+    Shape s;
+    int *status;
+    uint64_t timeout_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQc, const __grid_constant__ CUtensorMap tmGc,
+                   const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                   const DkvArgs args) {
+    using C = CfgK<D>;
+    constexpr int ST = C::ST;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const uint32_t sK = sbase + C::K_OFF, sV = sbase + C::V_OFF, sQ = sbase + C::Q_OFF,
+                   sG = sbase + C::G_OFF, sBar = sbase + C::BAR_OFF;
+    float *xvec = reinterpret_cast<float *>(smem + C::X_OFF);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NBARS * 8);
+    uint32_t *tmem_slot = misc;
+    volatile uint32_t *abort_flag = misc + 1;
+    auto bar = [&](int idx) -> uint32_t { return sBar + idx * 8; };
+
+    const Shape &s = args.s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtx wc{abort_flag, args.status, args.timeout_ns};
+
+    // ---- key block and its query chunks
+    const int nkb = (s.N + BK - 1) / BK;
+    const int kb = blockIdx.x % nkb;
+    const int bg = blockIdx.x / nkb;
+    const int g = bg % s.Hkv, b = bg / s.Hkv;
+    const int G = s.H / s.Hkv;
+    KWalk kw;
+    kw.j0 = kb * BK;
+    kw.period = s.period;
+    const int qlast = band_last_query(min(s.N - 1, kw.j0 + BK - 1), s.N, s.mode, s.k_local);
+    kw.n_band = (qlast - kw.j0) / QC + 1;
+    kw.m_first = 1;
+    kw.n_skip = 0;
+    if (s.mode == 0 && s.S > 0) {
+        kw.m_first = max(1, s.k_local / s.period + 1);
+        // multiples whose first skip query is inside the sequence
+        const int m_last = min(s.S, (s.N - 1 - kw.j0) / s.period);
+        kw.n_skip = 2 * max(0, m_last - kw.m_first + 1);
+    }
+    kw.per_head = kw.n_band + kw.n_skip;
+    const int n_chunks = G * kw.per_head;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_KV), 1);
+        for (int i = 0; i < ST; ++i) {
+            mbar_init(bar(C::B_QF + i), 1);
+            mbar_init(bar(C::B_QE + i), 1);
+            mbar_init(bar(C::B_XF + i), 32);
+            mbar_init(bar(C::B_XE + i), 128);
+        }
+        mbar_init(bar(C::B_SF), 1);
+        mbar_init(bar(C::B_PR), 128);
+        mbar_init(bar(C::B_BF), 1);
+        mbar_init(bar(C::B_OF), 1);
+        mbar_init(bar(C::B_DR), 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= producer: K and V tiles once, then Q/dO chunks
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmQc);
+            prefetch_tmap(&tmGc);
+            const uint64_t reused = policy_evict_last();
+            mbar_expect_tx(bar(C::B_KV), 2 * C::KT_BYTES);
+            for (int dc = 0; dc < C::KD; ++dc) {
+                tma_load_3d_hint(sK + dc * C::KT_DBLK, &tmK, dc * 64, kw.j0, b * s.Hkv + g, bar(C::B_KV), reused);
+                tma_load_3d_hint(sV + dc * C::KT_DBLK, &tmV, dc * 64, kw.j0, b * s.Hkv + g, bar(C::B_KV), reused);
+            }
+            int issued = 0;
+            for (int ci = 0; ci < n_chunks; ++ci) {
+                const int st = ci % ST, round = ci / ST;
+                if (round > 0 && !wait_bar(bar(C::B_QE + st), (round - 1) & 1, wc)) break;
+                int hh, i0, back;
+                bool sk;
+                kw.chunk(ci, hh, i0, back, sk);
+                const int plane = b * s.H + g * G + hh;
+                mbar_expect_tx(bar(C::B_QF + st), 2 * C::QC_BYTES);
+                for (int dc = 0; dc < C::KD; ++dc) {
+                    tma_load_3d_hint(sQ + st * C::QC_BYTES + dc * C::QC_DBLK, &tmQc, dc * 64, i0, plane,
+                                     bar(C::B_QF + st), reused);
+                    tma_load_3d_hint(sG + st * C::QC_BYTES + dc * C::QC_DBLK, &tmGc, dc * 64, i0, plane,
+                                     bar(C::B_QF + st), reused);
+                }
+                issued = ci + 1;
+            }
+            if (*abort_flag) {
+                volatile uint32_t zero = 0;
+                WaitCtx w2{&zero, nullptr, 20000000ull};
+                wait_bar(bar(C::B_KV), 0, w2);
+                for (int ci = max(0, issued - ST); ci < issued; ++ci)
+                    wait_bar(bar(C::B_QF + ci % ST), (ci / ST) & 1, w2);
+            }
+        }
+    } else if (warp == 2) {
+        // ================= per-query vectors of each chunk: bias = prior - lse (log2 units), D
+        bool ok = true;
+        for (int ci = 0; ok && ci < n_chunks; ++ci) {
+            const int st = ci % ST, round = ci / ST;
+            if (round > 0) {
+                ok = wait_bar(bar(C::B_XE + st), (round - 1) & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            int hh, i0, back;
+            bool sk;
+            kw.chunk(ci, hh, i0, back, sk);
+            const long long rbase = ((long long)b * s.H + g * G + hh) * s.N;
+            float *xb = xvec + st * 2 * QC;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = lane + 32 * e, i = i0 + c;
+                float bias = -INFINITY, dv = 0.f;
+                if (i < s.N) {
+                    const float lse2 = args.lse[rbase + i] * kLog2e;
+                    const float al = args.alpha ? args.alpha[rbase + i] : 1.f;
+                    const float prior = (s.mode != 0) ? 0.f : (sk ? log2f(1.f - al) : log2f(al));
+                    if (lse2 != -INFINITY) bias = prior - lse2;
+                    dv = args.Dws[rbase + i];
+                }
+                xb[c] = bias;
+                xb[QC + c] = dv;
+            }
+            mbar_arrive(bar(C::B_XF + st));
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0) {
+            bool ok = wait_bar(bar(C::B_KV), 0, wc);
+            const uint32_t idesc_t = idesc_bf16(BK, QC, 0, 0);  // S^T, dP^T: both operands K-major
+            const uint32_t idesc_a = idesc_bf16(BK, D, 0, 1);   // dV, dK: B = chunk, MN-major
+            for (int ci = 0; ok && ci < n_chunks; ++ci) {
+                const int st = ci % ST;
+                if (!wait_bar(bar(C::B_QF + st), (ci / ST) & 1, wc)) break;
+                // S^T / dP^T columns still hold the operands of chunk ci-1's dV/dK MMAs
+                if (ci >= 1 && !wait_bar(bar(C::B_BF), (ci - 1) & 1, wc)) break;
+                tc_fence_after();
+                const uint32_t q_st = sQ + st * C::QC_BYTES, g_st = sG + st * C::QC_BYTES;
+#pragma unroll
+                for (int dc = 0; dc < C::KD; ++dc) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc = (dc | ks) != 0;
+                        mma_ss(tbase + C::ST_COL, sdesc(sK + dc * C::KT_DBLK + ks * 32, 16, 1024),
+                               sdesc(q_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
+                        mma_ss(tbase + C::DPT_COL, sdesc(sV + dc * C::KT_DBLK + ks * 32, 16, 1024),
+                               sdesc(g_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
+                    }
+                }
+                tc_commit(bar(C::B_SF));
+                if (!wait_bar(bar(C::B_PR), ci & 1, wc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < QC / 16; ++kk) {
+                    const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tbase + C::DV_COL, tbase + C::ST_COL + kk * 8,
+                           sdesc(g_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
+                    mma_ts(tbase + C::DK_COL, tbase + C::DPT_COL + kk * 8,
+                           sdesc(q_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
+                }
+                tc_commit(bar(C::B_BF));
+                tc_commit(bar(C::B_QE + st));
+                if (ci == n_chunks - 1) tc_commit(bar(C::B_OF));
+            }
+            tc_commit(bar(C::B_DR));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp >= 4) {
+        // ================= one thread per key
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;
+        const int j = kw.j0 + r;
+        const bool key_ok = j < s.N;
+        const int qlast_j = key_ok ? band_last_query(j, s.N, s.mode, s.k_local) : -1;
+        const float sc = s.scale_log2;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        bool ok = true;
+
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int st = ci % ST;
+            ok = wait_bar(bar(C::B_SF), ci & 1, wc);
+            ok = ok && wait_bar(bar(C::B_XF + st), (ci / ST) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            int hh, i0, back;
+            bool sk;
+            kw.chunk(ci, hh, i0, back, sk);
+            // valid query columns of this key: [clo, chi]
+            int clo, chi;
+            if (!sk) {
+                clo = max(j - i0, 0);
+                chi = min(qlast_j - i0, QC - 1);
+            } else {
+                const int c = j + back - i0;
+                if (j + back < s.N && c >= 0 && c < QC) { clo = c; chi = c; }
+                else { clo = QC; chi = -1; }
+            }
+            if (!key_ok) { clo = QC; chi = -1; }
+            const float *xb = xvec + st * 2 * QC;
+#pragma unroll
+            for (int q = 0; q < QC / 16; ++q) {
+                uint32_t sr[16], dr[16];
+                tmem_ld16(tbase + lane_base + C::ST_COL + q * 16, sr);
+                tmem_ld16(tbase + lane_base + C::DPT_COL + q * 16, dr);
+                tmem_wait_ld();
+                uint32_t pp[8], pz[8];
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const int c0 = q * 16 + c;
+                    const float2 bias = *reinterpret_cast<const float2 *>(xb + c0);
+                    const float2 dd = *reinterpret_cast<const float2 *>(xb + QC + c0);
+                    const bool v0 = c0 >= clo && c0 <= chi, v1 = c0 + 1 >= clo && c0 + 1 <= chi;
+                    const float p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), sc, bias.x)) : 0.f;
+                    const float p1 = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, bias.y)) : 0.f;
+                    const float z0 = p0 * (__uint_as_float(dr[c]) - dd.x);
+                    const float z1 = p1 * (__uint_as_float(dr[c + 1]) - dd.y);
+                    pp[c / 2] = pack_bf16(p0, p1);
+                    pz[c / 2] = pack_bf16(z0, z1);
+                }
+                tmem_st8(tbase + lane_base + C::ST_COL + q * 8, pp);
+                tmem_st8(tbase + lane_base + C::DPT_COL + q * 8, pz);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PR));
+            mbar_arrive(bar(C::B_XE + st));
+        }
+
+        // ---- epilogue: dK * tau, dV -> bf16 -> shared (the K and V tiles) -> TMA store
+        if (ok) {
+            ok = wait_bar(bar(C::B_OF), 0, wc);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        const float tau = sc / kLog2e;
+        if (ok) {
+            tc_fence_after();
+            __syncwarp();
+#pragma unroll
+            for (int oc = 0; oc < D / 16; ++oc) {
+                uint32_t xk[16], xv[16];
+                tmem_ld16(tbase + lane_base + C::DK_COL + oc * 16, xk);
+                tmem_ld16(tbase + lane_base + C::DV_COL + oc * 16, xv);
+                tmem_wait_ld();
+                uint32_t pk[8], pv[8];
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    pk[c / 2] = pack_bf16(__uint_as_float(xk[c]) * tau, __uint_as_float(xk[c + 1]) * tau);
+                    pv[c / 2] = pack_bf16(__uint_as_float(xv[c]), __uint_as_float(xv[c + 1]));
+                }
+                const int dc = oc >> 2, quarter = oc & 3;
+                uint8_t *rk = smem + C::K_OFF + dc * C::KT_DBLK + r * ROW_BYTES;
+                uint8_t *rv = smem + C::V_OFF + dc * C::KT_DBLK + r * ROW_BYTES;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int off = ((quarter * 2 + w) ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(rk + off) = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    *reinterpret_cast<uint4 *>(rv + off) = make_uint4(pv[4 * w], pv[4 * w + 1], pv[4 * w + 2], pv[4 * w + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (ok && warp == 4 && lane == 0) {
+            const uint64_t once = policy_evict_first();
+            for (int dc = 0; dc < C::KD; ++dc) {
+                tma_store_3d(&tmDK, sK + dc * C::KT_DBLK, dc * 64, kw.j0, b * s.Hkv + g, once);
+                tma_store_3d(&tmDV, sV + dc * C::KT_DBLK, dc * 64, kw.j0, b * s.Hkv + g, once);
+            }
+            tma_store_commit_and_wait();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+static cudaError_t launch_dkdv(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mqc,
+                              const CUtensorMap &mgc, const CUtensorMap &mdk, const CUtensorMap &mdv,
+                              const DkvArgs &a, unsigned grid, cudaStream_t st) {
+    constexpr int smem = CfgK<D>::SMEM_BYTES;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    bwd_dkdv_tc_kernel<D><<<grid, NUM_THREADS, smem, st>>>(mk, mv, mqc, mgc, mdk, mdv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace tcb
+
+cudaError_t launch_bwd_dq_tc(const LaunchBwd &L, int *status, uint64_t timeout_ns, cudaStream_t st) {
+    using namespace tcb;
+    const Shape &s = L.s;
+    const int G = s.H / s.Hkv;
+    const int GP = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+    const int R = BM / GP;
+    CUtensorMap mq, mg, mk, mv, mdq;
+    if (!make_map(&mq, L.q, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mg, L.dout, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mdq, L.dq, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
+        !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
+        return cudaErrorNotSupported;
+    DqArgs a{L.alpha, L.lse, L.Dws, L.dalpha, s, GP, status, timeout_ns};
+    const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (s.d == 64) return launch_dq<64>(mq, mg, mk, mv, mdq, a, (unsigned)grid, st);
+    if (s.d == 128) return launch_dq<128>(mq, mg, mk, mv, mdq, a, (unsigned)grid, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dkdv_tc(const LaunchBwd &L, int *status, uint64_t timeout_ns, cudaStream_t st) {
+    using namespace tcb;
+    const Shape &s = L.s;
+    CUtensorMap mk, mv, mqc, mgc, mdk, mdv;
+    if (!make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
+        !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
+        !make_map(&mdk, L.dk, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
+        !make_map(&mdv, L.dv, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
+        !make_map(&mqc, L.q, s.d, s.N, (long long)s.B * s.H, QC, 1) ||
+        !make_map(&mgc, L.dout, s.d, s.N, (long long)s.B * s.H, QC, 1))
+        return cudaErrorNotSupported;
+    DkvArgs a{L.alpha, L.lse, L.Dws, s, status, timeout_ns};
+    const long long grid = (long long)s.B * s.Hkv * ((s.N + BK - 1) / BK);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (s.d == 64) return launch_dkdv<64>(mk, mv, mqc, mgc, mdk, mdv, a, (unsigned)grid, st);
+    if (s.d == 128) return launch_dkdv<128>(mk, mv, mqc, mgc, mdk, mdv, a, (unsigned)grid, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pi

@@ -29,6 +29,7 @@
 
 #include "pi_common.cuh"
 #include "pi_launch.h"
+#include "pi_tc_ptx.cuh"
 
 namespace pi {
 namespace tc {
@@ -73,253 +74,6 @@ struct Cfg {
     static constexpr int MISC_BYTES = NBARS * 8 + 16;
     static constexpr int SMEM_BYTES = BAR_OFF + MISC_BYTES + 1024;  // + alignment slack
 };
-
-// ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-struct WaitCtx {
-    volatile uint32_t *abort;
-    int *status;
-    uint64_t timeout_ns;
-};
-
-// Bounded wait on the phase of `bar` with the given parity.  Gives up when the
-// CTA's abort flag is raised, when another CTA has already recorded a failure in
-// the device status word (so a failing launch drains in one wave), or after
-// timeout_ns (then raises the flag and records the timeout).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx &w) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*w.abort) return false;
-        if (w.status && *reinterpret_cast<volatile int *>(w.status) != kStatusOk) {
-            *w.abort = 1u;
-            return false;
-        }
-        if (global_ns() - t0 > w.timeout_ns) {
-            *w.abort = 1u;
-            record_status(w.status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-// Same with an L2 cache policy (createpolicy) attached to the transfer.
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
-                                                 uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int x, int y, int z,
-                                             uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
-        " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tm)),
-        "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ void tma_store_commit_and_wait() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// tcgen05
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-#define PI_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
-                 "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : PI_R8(0), PI_R8(8), PI_R8(16), PI_R8(24)
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : PI_R8(0), PI_R8(8)
-        : "r"(taddr));
-}
-#undef PI_R8
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
-    tmem_st16(taddr, v);
-    tmem_st16(taddr + 16, v + 16);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
-
-// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction for two lanes of work).
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// f[x] for a runtime index x in [0, 32) without local memory: a select tree on x's bits.
-__device__ __forceinline__ float select32(const float *f, int x) {
-    float a[16], b[8], c[4], d[2];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) a[j] = (x & 1) ? f[2 * j + 1] : f[2 * j];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = (x & 2) ? a[2 * j + 1] : a[2 * j];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) c[j] = (x & 4) ? b[2 * j + 1] : b[2 * j];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) d[j] = (x & 8) ? c[2 * j + 1] : c[2 * j];
-    return (x & 16) ? d[1] : d[0];
-}
-
-// 2^x on the FMA pipe instead of the MUFU pipe: x = n + f with n = round(x) and f in
-// [-1/2, 1/2]; 2^f from a degree-3 polynomial (coefficients fitted by fit_exp2_poly.py next
-// to this file, max relative error 7.5e-5, far below the 2^-9 of the bf16 P it feeds) and
-// 2^n added into the exponent field.  Exactly 0 below 2^-126, like the masked logits need.
-__device__ __forceinline__ float exp2_poly(float x) {
-    const float xc = fmaxf(x, -126.f);
-    const float t = xc + 12582912.f;  // 1.5 * 2^23: the low bits of t now hold round(xc)
-    const float n = t - 12582912.f;
-    const float f = xc - n;
-    const float p = fmaf(fmaf(fmaf(0.0551716573536396f, f, 0.2426111400127411f), f,
-                              0.6932609677314758f), f, 0.9999280571937561f);
-    const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-    return (x < -126.f) ? 0.f : r;
-}
-
-#ifndef PI_EXP2_POLY_EVERY
-#define PI_EXP2_POLY_EVERY 0  // 0: every exp2 on MUFU; k > 0: one column pair in k on the FMA pipe
-#endif
 
 // Phase 1 of a key chunk for one row: mask the scores outside [clo, chi] and return the
 // chunk's largest logit in log2 units (prior included).  A skip chunk holds at most one
@@ -368,15 +122,8 @@ __device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, f
     for (int c = 0; c < 32; c += 2) {
         float z0, z1;
         unpack2(fma2(pack2(f[c], f[c + 1]), sc2, bo2), z0, z1);
-        float p0, p1;
-        if (PI_EXP2_POLY_EVERY > 0 && ((c >> 1) % (PI_EXP2_POLY_EVERY > 0 ? PI_EXP2_POLY_EVERY : 1)) ==
-                                          (PI_EXP2_POLY_EVERY > 0 ? PI_EXP2_POLY_EVERY - 1 : 0)) {
-            p0 = exp2_poly(z0);
-            p1 = exp2_poly(z1);
-        } else {
-            p0 = fast_exp2(z0);
-            p1 = fast_exp2(z1);
-        }
+        const float p0 = fast_exp2(z0);
+        const float p1 = fast_exp2(z1);
         if ((c >> 1) & 1) acc1 = add2(acc1, pack2(p0, p1));
         else acc0 = add2(acc0, pack2(p0, p1));
         pk[c / 2] = pack_bf16(p0, p1);
@@ -385,23 +132,6 @@ __device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, f
     unpack2(acc0, a0, a1);
     unpack2(acc1, b0, b1);
     return (a0 + a1) + (b0 + b1);
-}
-
-// Shared-memory matrix descriptor (tcgen05): start, leading and stride byte
-// offsets, descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, M x N, operand majors.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -893,40 +623,6 @@ __global__ void wait_timeout_probe_kernel(int *status, uint64_t timeout_ns) {
 }
 
 // ------------------------------------------------------------------ host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 3-D bf16 tensor map over [planes][rows][d] with a (64, box_rows, box_planes) box, 128B swizzle.
-static bool make_map(CUtensorMap *m, const void *ptr, int d, int rows, long long planes, int box_rows,
-                     int box_planes) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)rows};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int D, int DBG>
 static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,

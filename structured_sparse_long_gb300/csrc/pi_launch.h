@@ -42,6 +42,14 @@ struct LaunchBwd {
 // CUDA-core kernels (pi_simt.cu)
 cudaError_t launch_fwd_simt(const LaunchFwd &L, cudaStream_t st);
 cudaError_t launch_bwd_simt(const LaunchBwd &L, cudaStream_t st);
+// key-major dk/dv pass alone; reads D_i from L.Dws (pi_simt.cu)
+cudaError_t launch_bwd_dkdv_simt(const LaunchBwd &L, cudaStream_t st);
+
+// tcgen05 backward, bf16, d in {64, 128} (pi_bwd_tc.cu): query-major pass writing dq,
+// D_i (into L.Dws) and dalpha
+cudaError_t launch_bwd_dq_tc(const LaunchBwd &L, int *status, uint64_t timeout_ns, cudaStream_t st);
+// key-major pass writing dk and dv from D_i in L.Dws (pi_bwd_tc.cu)
+cudaError_t launch_bwd_dkdv_tc(const LaunchBwd &L, int *status, uint64_t timeout_ns, cudaStream_t st);
 
 // tcgen05 / TMEM / TMA forward, bf16, d in {64, 128} (pi_fwd_tc.cu).
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.

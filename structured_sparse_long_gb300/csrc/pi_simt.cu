@@ -379,6 +379,14 @@ static cudaError_t bwd_run(const BwdArgs &a, const Shape &s, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+template <typename T, int D>
+static cudaError_t dkdv_run(const BwdArgs &a, const Shape &s, cudaStream_t st) {
+    const long long krows = (long long)s.B * s.Hkv * s.N;
+    const dim3 g2((unsigned)((krows + kWarps - 1) / kWarps));
+    bwd_dkdv_kernel<T, D><<<g2, kWarps * 32, 0, st>>>(a, s);
+    return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t bwd_dispatch(const BwdArgs &a, const Shape &s, cudaStream_t st) {
     switch (s.d) {
@@ -395,6 +403,18 @@ cudaError_t launch_fwd_simt(const LaunchFwd &L, cudaStream_t st) {
     simt::FwdArgs a{L.q, L.k, L.v, L.alpha, L.out, L.lse, L.cnt, L.isum, L.lse_in, L.P};
     if (L.fp32) return simt::fwd_dispatch<float>(a, L.s, L.dbg, st);
     return simt::fwd_dispatch<__nv_bfloat16>(a, L.s, L.dbg, st);
+}
+
+cudaError_t launch_bwd_dkdv_simt(const LaunchBwd &L, cudaStream_t st) {
+    simt::BwdArgs a{L.q, L.k, L.v, L.alpha, L.out, L.lse, L.dout, L.dq, L.dk, L.dv, L.dalpha,
+                    L.Dws};
+    if (L.fp32) return cudaErrorInvalidValue;
+    switch (L.s.d) {
+        case 32: return simt::dkdv_run<__nv_bfloat16, 32>(a, L.s, st);
+        case 64: return simt::dkdv_run<__nv_bfloat16, 64>(a, L.s, st);
+        case 128: return simt::dkdv_run<__nv_bfloat16, 128>(a, L.s, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_bwd_simt(const LaunchBwd &L, cudaStream_t st) {
