@@ -114,7 +114,7 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
         if (!status) return PI_ERR_CUDA;
         const cudaError_t e = pi::launch_bwd_dq_tc(L, status, kWaitTimeoutNs, st);
         if (e != cudaSuccess) return PI_ERR_CUDA;
-        return map_cuda(pi::launch_bwd_dkdv_simt(L, st));
+        return map_cuda(pi::launch_bwd_dkdv_tc(L, status, kWaitTimeoutNs, st));
     }
     return map_cuda(pi::launch_bwd_simt(L, st));
 }
