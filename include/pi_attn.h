@@ -215,7 +215,7 @@ int pi_attn_debug_probs(const void *q, const void *k, const void *v, const float
  * pi_attn_debug_trace -- runs the bf16 tcgen05 forward (d = 64 or 128; writes out
  * and lse as pi_attn_fwd does) and records, for CTAs 0 .. n_trace_ctas-1, the
  * SM cycle counter (clock64) at the pipeline events of each CTA into
- * trace [n_trace_ctas][232] int64 (caller-owned, zero-filled by the caller):
+ * trace [n_trace_ctas][240] int64 (caller-owned, zero-filled by the caller):
  *   slot 0 entry, 1 set-up done, 2 Q load issued, 3 Q landed (seen by the S
  *   issuer), 4 O complete (seen by the epilogue), 5 output stored, 6 exit,
  *   7 number of key tiles; for tile t < 16: 8+t K load issued, 24+t V load
@@ -224,8 +224,9 @@ int pi_attn_debug_probs(const void *q, const void *k, const void *v, const float
  *   one thread: 104+t S issuer waiting for K, 120+t S issuer waiting for its
  *   TMEM buffer, 136+t PV issuer waiting for P, 152+t PV issuer waiting for V,
  *   168+t softmax waiting for S; softmax stamps inside tile t: 184+t S loaded
- *   from TMEM, 200+t maxima done, 216+t P stored to TMEM.  Stamps of different
- *   warps need not share a clock.  A profiling aid; the pages define no such
+ *   from TMEM, 200+t maxima done, 216+t P stored to TMEM; 232 the SM id, 233
+ *   and 234 the global timer (ns) at entry and exit.  Stamps of different warps
+ *   need not share a clock.  A profiling aid; the pages define no such
  *   operation.
  */
 int pi_attn_debug_trace(const void *q, const void *k, const void *v, const float *alpha,

@@ -231,11 +231,11 @@ def debug_probs(q, k, v, alpha, lse_in, k_local, period, S, mode=MODE_PI, stream
 
 
 def debug_trace(q, k, v, alpha, k_local, period, S, mode=MODE_PI, n_ctas=256, stream=None):
-    """pi_attn_debug_trace. Returns (out, lse, trace int64 [n_ctas, 232]) of clock64 stamps."""
+    """pi_attn_debug_trace. Returns (out, lse, trace int64 [n_ctas, 240]) of clock64 stamps."""
     B, H, Hkv, N, d = _sizes(q, k)
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
-    trace = torch.zeros((n_ctas, 232), device=q.device, dtype=torch.int64)
+    trace = torch.zeros((n_ctas, 240), device=q.device, dtype=torch.int64)
     rc = load().pi_attn_debug_trace(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d,
                                     k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(trace),
                                     n_ctas, _stream(stream))

@@ -17,8 +17,8 @@
 //     chunks; each row attends to exactly one column of it (the "diagonal").
 //     Two chunks make one key tile (N <= 64).
 //   * Warp 0 (lane 0) streams Q and K tiles with TMA, warp 2 (lane 0) streams V
-//     tiles; warp 1 (lane 0) issues tcgen05.mma: S = Q K^T into one of two
-//     64-column TMEM buffers, then O += P V with P read from TMEM.
+//     tiles; warp 1 (lane 0) issues S = Q K^T into one of two 64-column TMEM
+//     buffers, warp 3 (lane 0) issues O += P V with P read from TMEM.
 //   * Warps 4-7 run the softmax, one thread per row (TMEM lane = row): masks,
 //     adds the prior, keeps the running max m and sum l (rescaling O in TMEM
 //     only when the max grows by more than 2^8), writes P as bf16 over its S,
@@ -55,24 +55,28 @@ struct Cfg {
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + Q_BYTES;
     static constexpr int V_OFF = K_OFF + STAGES * KV_STAGE;
-    static constexpr int BAR_OFF = V_OFF + STAGES * KV_STAGE;
+    static constexpr int DATA_BYTES = V_OFF + STAGES * KV_STAGE;  // from a 1024-byte aligned base
     // barrier indices
     static constexpr int B_Q = 0;
     static constexpr int B_KF = 1;
     static constexpr int B_KE = B_KF + STAGES;
     static constexpr int B_VF = B_KE + STAGES;
     static constexpr int B_VE = B_VF + STAGES;
-    static constexpr int B_SF = B_VE + STAGES;
-    static constexpr int B_PR = B_SF + 2;
-    // PV of tile U completes barrier B_PV + (U & 1), phase U >> 1: with two barriers no
+    static constexpr int B_SF = B_VE + STAGES;  // S of the tile in TMEM buffer t & 1
+    static constexpr int B_PR = B_SF + 2;       // P of the tile written over its S
+    // PV of tile T completes barrier B_PV + (T & 1), phase T >> 1: with two barriers no
     // parity wait ever has two of its phases outstanding.
     static constexpr int B_PV = B_PR + 2;
     static constexpr int B_OF = B_PV + 2;  // O complete (after the last PV), single phase
     static constexpr int B_DR = B_OF + 1;  // drain of the S issuer's MMAs
     static constexpr int B_DR2 = B_DR + 1; // drain of the PV issuer's MMAs
     static constexpr int NBARS = B_DR2 + 1;
-    static constexpr int MISC_BYTES = NBARS * 8 + 16;
-    static constexpr int SMEM_BYTES = BAR_OFF + MISC_BYTES + 1024;  // + alignment slack
+    static constexpr int BAR_BYTES = NBARS * 8 + 16;  // + TMEM address and abort flag
+    static_assert(BAR_BYTES <= 512, "barriers must fit the alignment gap or its complement");
+    // The data starts at the first 1024-byte boundary of the dynamic shared memory; the
+    // barriers go into the gap before it when it is large enough, else after the data.
+    // Either way DATA_BYTES + 1024 bytes suffice.
+    static constexpr int SMEM_BYTES = DATA_BYTES + 1024;
 };
 
 // Phase 1 of a key chunk for one row: mask the scores outside [clo, chi] and return the
@@ -134,13 +138,59 @@ __device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, f
     return (a0 + a1) + (b0 + b1);
 }
 
+// Fast path of a key tile that lies inside the band of every row: P = exp2(f * sc + bo) for
+// the tile's 64 scores, packed as bf16 pairs in place (word c/2 of each chunk, written after
+// scores c and c+1 were read); returns the sum of the fp32 values.
+__device__ __forceinline__ float exp_pack64(uint32_t *ra, uint32_t *rb, float sc, float bo) {
+    const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo);
+    uint64_t acc[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t *r = h ? rb : ra;
+#pragma unroll
+        for (int c = 0; c < CHUNK; c += 2) {
+            float z0, z1;
+            unpack2(fma2(pack2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), sc2, bo2), z0, z1);
+            const float p0 = fast_exp2(z0), p1 = fast_exp2(z1);
+            acc[2 * h + ((c >> 1) & 1)] = add2(acc[2 * h + ((c >> 1) & 1)], pack2(p0, p1));
+            r[c / 2] = pack_bf16(p0, p1);
+        }
+    }
+    float a[8];
+    unpack2(acc[0], a[0], a[1]);
+    unpack2(acc[1], a[2], a[3]);
+    unpack2(acc[2], a[4], a[5]);
+    unpack2(acc[3], a[6], a[7]);
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
+// Largest of the 64 raw scores of a tile (eight independent chains).
+__device__ __forceinline__ float max64(const uint32_t *ra, const uint32_t *rb) {
+    float m[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        m[k] = max3(__uint_as_float(ra[k]), __uint_as_float(ra[k + 4]), __uint_as_float(ra[k + 8]));
+        m[k + 4] = max3(__uint_as_float(rb[k]), __uint_as_float(rb[k + 4]), __uint_as_float(rb[k + 8]));
+    }
+#pragma unroll
+    for (int c = 12; c < CHUNK; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[k] = max3(m[k], __uint_as_float(ra[c + k]), __uint_as_float(ra[c + 4 + k]));
+            m[k + 4] = max3(m[k + 4], __uint_as_float(rb[c + k]), __uint_as_float(rb[c + 4 + k]));
+        }
+    }
+    return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], max3(m[4], m[5], m[6]), m[7]));
+}
+
 // ------------------------------------------------------------------ kernel
 
 struct TcArgs {
     const float *alpha;
     float *lse;
     Shape s;
-    int GP;  // query heads packed per CTA
+    int GP;       // query heads packed per CTA
+    int m_first;  // smallest skip multiple m with m * period > k_local
     int *status;
     uint64_t timeout_ns;
     int *cnt;
@@ -156,10 +206,12 @@ struct TcArgs {
 // (t < 16): 8+t K issued, 24+t V issued, 40+t S issued, 56+t PV issued, 72+t S seen by the
 // softmax, 88+t P ready; and cycles spent waiting, each measured within one thread:
 // 104+t S issuer on K, 120+t S issuer on the S buffer (PV of t-2), 136+t PV issuer on P,
-// 152+t PV issuer on V, 168+t softmax on S; softmax (warp 4) stamps inside tile t:
-// 184+t S loaded from TMEM, 200+t masked maxima done, 216+t P stored to TMEM (issued).
-// Absolute stamps of different warps need not share a clock; the waits are exact.
-constexpr int kTraceSlots = 232;
+// 152+t PV issuer on V, 168+t softmax on S; softmax (warp 4) stamps inside tile t: 184+t S
+// loaded from TMEM, 200+t maxima done (full tiles: exponentials done), 216+t P written to
+// TMEM (issued); 232 the SM the CTA ran on, 233 and 234 the global timer (ns) at
+// entry and exit.  Absolute stamps of different warps need not share a clock; the waits are
+// exact.
+constexpr int kTraceSlots = 240;
 constexpr int kTraceTiles = 16;
 
 // Key chunk ci of the block: first key position, whether it is a skip chunk,
@@ -192,9 +244,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw_addr + pad;
+    const uint32_t bar_off = (pad >= (uint32_t)C::BAR_BYTES) ? 0u : pad + C::DATA_BYTES;
     const uint32_t sQ = sbase + C::Q_OFF, sK = sbase + C::K_OFF, sV = sbase + C::V_OFF;
-    const uint32_t sBar = sbase + C::BAR_OFF;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::BAR_OFF + C::NBARS * 8);
+    const uint32_t sBar = raw_addr + bar_off;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem_raw + bar_off + C::NBARS * 8);
     uint32_t *tmem_slot = misc;
     volatile uint32_t *abort_flag = misc + 1;
     auto bar = [&](int idx) -> uint32_t { return sBar + idx * 8; };
@@ -202,9 +255,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const Shape &s = args.s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const WaitCtx wc{abort_flag, args.status, args.timeout_ns};
+    // grid (position block, head group, batch entry): positions fastest, as CTAs are launched
+    const long long lin = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    const bool traced = DBG == 3 && lin < args.n_trace;
     auto stamp = [&](int slot) {
-        if (DBG == 3 && (int)blockIdx.x < args.n_trace)
-            args.trace[(long long)blockIdx.x * kTraceSlots + slot] = (long long)clock64();
+        if (traced) args.trace[lin * kTraceSlots + slot] = (long long)clock64();
     };
     auto stamp_tile = [&](int base, int t) {
         if (t < kTraceTiles) stamp(base + t);
@@ -213,23 +268,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     auto timed_wait = [&](uint32_t b, uint32_t parity, int slot_base, int t) -> bool {
         const long long c0 = (DBG == 3) ? (long long)clock64() : 0;
         const bool r = wait_bar(b, parity, wc);
-        if (DBG == 3 && t < kTraceTiles && (int)blockIdx.x < args.n_trace)
-            args.trace[(long long)blockIdx.x * kTraceSlots + slot_base + t] = (long long)clock64() - c0;
+        if (traced && t < kTraceTiles) args.trace[lin * kTraceSlots + slot_base + t] = (long long)clock64() - c0;
         return r;
     };
-    if (threadIdx.x == 0) stamp(0);
+    if (threadIdx.x == 0 && traced) {
+        stamp(0);
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        args.trace[lin * kTraceSlots + 232] = smid;
+        args.trace[lin * kTraceSlots + 233] = (long long)global_ns();
+    }
 
-    // ---- block coordinates: (b, head group, position block), positions fastest
+    // ---- block coordinates
     const int GP = args.GP;
     const int R = BM / GP;
-    const int nqb = (s.N + R - 1) / R;
-    const int hsub = s.H / GP;
-    int bid = blockIdx.x;
-    const int pb = bid % nqb;
-    bid /= nqb;
-    const int hs = bid % hsub;
-    const int b = bid / hsub;
-    const int h0 = hs * GP;
+    const int pb = blockIdx.x, b = blockIdx.z;
+    const int h0 = blockIdx.y * GP;
     const int g = h0 / (s.H / s.Hkv);
     const int p0 = pb * R;
 
@@ -243,14 +297,23 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int band_hi = min(s.N - 1, p0 + R - 1);
     cw.n_band = (band_hi - cw.lo0) / CHUNK + 1;
     int n_skip_blocks = 0;
-    cw.m_first = 1;
+    cw.m_first = args.m_first;
     if (s.mode == 0 && s.S > 0) {
-        cw.m_first = max(1, s.k_local / s.period + 1);  // smallest m with m*period > k
         const int m_last = min(s.S, (p0 + R - 1) / s.period);
         n_skip_blocks = max(0, m_last - cw.m_first + 1);
     }
     const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
     const int n_tiles = (n_chunks + 1) / 2;
+    // Band chunks full_lo .. full_hi lie inside the band of every row of the block (the block
+    // has no rows past N, the chunk starts at or after the last row's first key and ends at or
+    // before the first row): such chunks need no per-row range.
+    int full_lo = 1, full_hi = 0;
+    if (p0 + R <= s.N) {
+        const int lo_last = band_lo(p0 + R - 1, s.mode, s.k_local);
+        full_lo = (lo_last - cw.lo0 + CHUNK - 1) / CHUNK;
+        const int span = p0 - (CHUNK - 1) - cw.lo0;
+        full_hi = span >= 0 ? min(span / CHUNK, cw.n_band - 1) : -1;
+    }
 
     // ---- setup: barriers, TMEM
     if (threadIdx.x == 0) {
@@ -280,8 +343,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tbase = *tmem_slot;
     if (threadIdx.x == 0) {
         stamp(1);
-        if (DBG == 3 && (int)blockIdx.x < args.n_trace)
-            args.trace[(long long)blockIdx.x * kTraceSlots + 7] = n_tiles;
+        if (traced) args.trace[lin * kTraceSlots + 7] = n_tiles;
     }
 
     if (warp == 0) {
@@ -450,6 +512,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         };
 
+        // Rescale this row of O when the reference max moved.  PV of tile t-1 must be done.
+        // The wait names that phase exactly: S of tile t-1 implied PV of tile t-3 finished,
+        // and PV of tile t+1 cannot start before this thread arrives for tile t+1.
+        auto rescale_o = [&](int t, bool need_o, float corr) -> bool {
+            if (!__any_sync(0xffffffffu, need_o)) return true;
+            const bool r_ = wait_bar(bar(C::B_PV + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc);
+            if (!__all_sync(0xffffffffu, r_)) return false;
+            tc_fence_after();
+            const float f = need_o ? corr : 1.f;
+#pragma unroll
+            for (int oc = 0; oc < D / 16; ++oc) {
+                uint32_t x[16];
+                tmem_ld16(tbase + lane_base + O_COL + oc * 16, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * f);
+                tmem_st16(tbase + lane_base + O_COL + oc * 16, x);
+            }
+            return true;
+        };
+
         for (int t = 0; t < n_tiles; ++t) {
             const int buf = t & 1;
             if (warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (t >> 1) & 1, 168, t);
@@ -467,76 +550,84 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tmem_wait_ld();
             if (warp == 4 && lane == 0) stamp_tile(184, t);
 
-            int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
-            float offa, offb = 0.f;
-            bool ska, skb = false;
-            chunk_range(2 * t, key0a, cloa, chia, offa, ska);
-            if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb, skb);
-
-            float *fa = reinterpret_cast<float *>(ra);
-            float *fb = reinterpret_cast<float *>(rb);
-            const float za = chunk_max(fa, cloa, chia, ska, sc, offa);
-            const float zb = (nch > 1) ? chunk_max(fb, clob, chib, skb, sc, offb) : -INFINITY;
-            const float mt = fmaxf(za, zb);
-            if (warp == 4 && lane == 0) stamp_tile(200, t);
-            float corr = 1.f;
+            // Full tile (the same for every thread of the CTA): P with the running reference; the
+            // maximum is only needed when some P exceeds 2^8 (the lazy-rescale bound), which a
+            // sum above 2^8 is the first sign of.  Rows with no reference yet take the general
+            // path, as do the debug modes that record per-row ranges.
+            const bool fast = (DBG == 0 || DBG == 3) && nch == 2 && 2 * t >= full_lo && 2 * t + 1 <= full_hi &&
+                              __all_sync(0xffffffffu, m_ref != -INFINITY);
+            float corr = 1.f, lsum;
             bool need_o = false;
-            if (mt > m_ref + kRescaleThreshold) {
-                if (m_ref != -INFINITY) {
-                    corr = fast_exp2(m_ref - mt);
-                    need_o = (t > 0);
+            if (fast) {
+                lsum = exp_pack64(ra, rb, sc, off_band - m_ref);
+                if (__any_sync(0xffffffffu, !(lsum <= 256.f))) {
+                    tmem_ld32(tS, ra);  // S is still in TMEM: P has not been written yet
+                    tmem_ld32(tS + CHUNK, rb);
+                    tmem_wait_ld();
+                    const float mt = fmaf(max64(ra, rb), sc, off_band);
+                    if (mt > m_ref + kRescaleThreshold) {
+                        corr = fast_exp2(m_ref - mt);
+                        need_o = true;  // m_ref was set by an earlier tile, so t > 0
+                        m_ref = mt;
+                    }
+                    l *= corr;
+                    lsum = exp_pack64(ra, rb, sc, off_band - m_ref);
                 }
-                m_ref = mt;
-            }
-            l *= corr;
-            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+                if (warp == 4 && lane == 0) stamp_tile(200, t);
+                tmem_st16(tS, ra);
+                tmem_st16(tS + CHUNK / 2, rb);
+            } else {
 
-            if (DBG == 1) {
-                const int na = max(0, chia - cloa + 1), nb = max(0, chib - clob + 1);
-                cnt += na + nb;
-                isum += (long long)na * key0a + (long long)(cloa + chia) * na / 2;
-                isum += (long long)nb * key0b + (long long)(clob + chib) * nb / 2;
-            }
-            if (DBG == 2 && row_ok && lse2_in != -INFINITY) {
-                for (int c = 0; c < CHUNK; ++c) {
-                    if (c >= cloa && c <= chia)
-                        args.P[row_g * s.N + key0a + c] = exp2f(fmaf(fa[c], sc, offa - lse2_in));
-                    if (nch > 1 && c >= clob && c <= chib)
-                        args.P[row_g * s.N + key0b + c] = exp2f(fmaf(fb[c], sc, offb - lse2_in));
+                int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
+                float offa, offb = 0.f;
+                bool ska, skb = false;
+                chunk_range(2 * t, key0a, cloa, chia, offa, ska);
+                if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb, skb);
+
+                float *fa = reinterpret_cast<float *>(ra);
+                float *fb = reinterpret_cast<float *>(rb);
+                const float za = chunk_max(fa, cloa, chia, ska, sc, offa);
+                const float zb = (nch > 1) ? chunk_max(fb, clob, chib, skb, sc, offb) : -INFINITY;
+                const float mt = fmaxf(za, zb);
+                if (warp == 4 && lane == 0) stamp_tile(200, t);
+                if (mt > m_ref + kRescaleThreshold) {
+                    if (m_ref != -INFINITY) {
+                        corr = fast_exp2(m_ref - mt);
+                        need_o = (t > 0);
+                    }
+                    m_ref = mt;
                 }
-            }
+                l *= corr;
+                const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-            // P = exp2(z - m_ref) as bf16, written over the chunk's S columns
-            uint32_t pk[CHUNK / 2];
-            float lsum = chunk_exp(fa, cloa, ska, za, sc, offa, mu, pk);
-            tmem_st16(tS, pk);
-            if (nch > 1) {
-                lsum += chunk_exp(fb, clob, skb, zb, sc, offb, mu, pk);
-                tmem_st16(tS + CHUNK / 2, pk);
+                if (DBG == 1) {
+                    const int na = max(0, chia - cloa + 1), nb = max(0, chib - clob + 1);
+                    cnt += na + nb;
+                    isum += (long long)na * key0a + (long long)(cloa + chia) * na / 2;
+                    isum += (long long)nb * key0b + (long long)(clob + chib) * nb / 2;
+                }
+                if (DBG == 2 && row_ok && lse2_in != -INFINITY) {
+                    for (int c = 0; c < CHUNK; ++c) {
+                        if (c >= cloa && c <= chia)
+                            args.P[row_g * s.N + key0a + c] = exp2f(fmaf(fa[c], sc, offa - lse2_in));
+                        if (nch > 1 && c >= clob && c <= chib)
+                            args.P[row_g * s.N + key0b + c] = exp2f(fmaf(fb[c], sc, offb - lse2_in));
+                    }
+                }
+
+                // P = exp2(z - m_ref) as bf16, written over the chunk's S columns
+                uint32_t pk[CHUNK / 2];
+                lsum = chunk_exp(fa, cloa, ska, za, sc, offa, mu, pk);
+                tmem_st16(tS, pk);
+                if (nch > 1) {
+                    lsum += chunk_exp(fb, clob, skb, zb, sc, offb, mu, pk);
+                    tmem_st16(tS + CHUNK / 2, pk);
+                }
             }
             if (warp == 4 && lane == 0) stamp_tile(216, t);
             l += lsum;
             __syncwarp();
-
-            // Rescale this row of O when the reference max moved.  PV of tile t-1 must be done.
-            // The wait names that phase exactly: S of tile t-1 implied PV of tile t-3 finished,
-            // and PV of tile t+1 cannot start before this thread arrives for tile t+1.
-            if (__any_sync(0xffffffffu, need_o)) {
-                ok = wait_bar(bar(C::B_PV + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                const float f = need_o ? corr : 1.f;
-#pragma unroll
-                for (int oc = 0; oc < D / 16; ++oc) {
-                    uint32_t x[16];
-                    tmem_ld16(tbase + lane_base + O_COL + oc * 16, x);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * f);
-                    tmem_st16(tbase + lane_base + O_COL + oc * 16, x);
-                }
-            }
+            if (!rescale_o(t, need_o, corr)) { ok = false; break; }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_PR + buf));
@@ -557,20 +648,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_after();
             __syncwarp();
 #pragma unroll
-            for (int oc = 0; oc < D / 16; ++oc) {  // 16 fp32 columns -> two 16-byte chunks
-                uint32_t x[16];
-                tmem_ld16(tbase + lane_base + O_COL + oc * 16, x);
+            for (int oh = 0; oh < D / 32; ++oh) {  // 32 fp32 columns per TMEM round trip
+                uint32_t x[32];
+                tmem_ld32(tbase + lane_base + O_COL + oh * 32, x);
                 tmem_wait_ld();
-                uint32_t pk[8];
-#pragma unroll
-                for (int c = 0; c < 16; c += 2)
-                    pk[c / 2] = pack_bf16(__uint_as_float(x[c]) * inv_l, __uint_as_float(x[c + 1]) * inv_l);
-                const int dc = oc >> 2, quarter = oc & 3;
+                const int dc = oh >> 1;
                 uint8_t *rowp = smem + C::Q_OFF + dc * C::Q_DBLK + r * ROW_BYTES;
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int cidx = quarter * 2 + w;
-                    uint4 val = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                for (int w = 0; w < 4; ++w) {  // 8 columns -> one 16-byte chunk of the row
+                    const int cidx = (oh & 1) * 4 + w;
+                    const float *f = reinterpret_cast<const float *>(x) + 8 * w;
+                    const uint4 val = make_uint4(pack_bf16(f[0] * inv_l, f[1] * inv_l), pack_bf16(f[2] * inv_l, f[3] * inv_l),
+                                                 pack_bf16(f[4] * inv_l, f[5] * inv_l), pack_bf16(f[6] * inv_l, f[7] * inv_l));
                     *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (r & 7)) << 4)) = val;
                 }
             }
@@ -596,7 +685,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ---- teardown
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) stamp(6);
+    if (threadIdx.x == 0 && traced) {
+        stamp(6);
+        args.trace[lin * kTraceSlots + 234] = (long long)global_ns();
+    }
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
@@ -626,7 +718,7 @@ __global__ void wait_timeout_probe_kernel(int *status, uint64_t timeout_ns) {
 
 template <int D, int DBG>
 static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          const CUtensorMap &mo, const TcArgs &a, unsigned grid, cudaStream_t st) {
+                          const CUtensorMap &mo, const TcArgs &a, dim3 grid, cudaStream_t st) {
     constexpr int smem = Cfg<D>::SMEM_BYTES;
     static int configured_device = -1;
     int dev = 0;
@@ -655,21 +747,23 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
-    TcArgs a{L.alpha, L.lse, s, GP, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P,
+    int m_first = 1;
+    if (s.mode == 0 && s.S > 0) m_first = s.k_local / s.period + 1;  // smallest m with m*period > k
+    TcArgs a{L.alpha, L.lse, s, GP, m_first, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P,
              L.trace, L.n_trace};
-    const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (s.H / GP > 65535 || s.B > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)((s.N + R - 1) / R), (unsigned)(s.H / GP), (unsigned)s.B);
     if (s.d == 64) {
-        if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        if (L.dbg == 3) return launch<64, 3>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        return launch<64, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 3) return launch<64, 3>(mq, mk, mv, mo, a, grid, st);
+        return launch<64, 2>(mq, mk, mv, mo, a, grid, st);
     }
     if (s.d == 128) {
-        if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        if (L.dbg == 3) return launch<128, 3>(mq, mk, mv, mo, a, (unsigned)grid, st);
-        return launch<128, 2>(mq, mk, mv, mo, a, (unsigned)grid, st);
+        if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 3) return launch<128, 3>(mq, mk, mv, mo, a, grid, st);
+        return launch<128, 2>(mq, mk, mv, mo, a, grid, st);
     }
     return cudaErrorInvalidValue;
 }
