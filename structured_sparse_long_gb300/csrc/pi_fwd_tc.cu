@@ -336,6 +336,33 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         *abort_flag = 0u;
         fence_barrier_init();
     }
+    // K and V tile t into ring stage t % ST (the stage must be free)
+    auto issue_kv = [&](const CUtensorMap *tm, uint32_t sbuf, int full_bar, int t, uint64_t policy) {
+        const int st = t % ST;
+        const int nch = min(2, n_chunks - 2 * t);
+        mbar_expect_tx(bar(full_bar + st), nch * C::KD * BOX_BYTES);
+        for (int cc = 0; cc < nch; ++cc) {
+            int back, u;
+            bool sk;
+            const int key0 = cw.key0(2 * t + cc, back, u, sk);
+            for (int dc = 0; dc < C::KD; ++dc)
+                tma_load_3d_hint(sbuf + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, tm, dc * 64,
+                                 key0, b * s.Hkv + g, bar(full_bar + st), policy);
+        }
+    };
+    // Q and the first K tile, which the first S = Q K^T waits for, go out before the CTA
+    // barrier, so that their latency overlaps the TMEM allocation and the barrier itself.
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
+        for (int dc = 0; dc < C::KD; ++dc)
+            tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
+                             policy_evict_first());
+        stamp(2);
+        stamp_tile(8, 0);
+        issue_kv(&tmK, sK, C::B_KF, 0, policy_evict_last());
+    }
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -347,31 +374,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 
     if (warp == 0) {
-        // ================= producer: Q and K tiles
+        // ================= producer: K tiles after the first
         if (lane == 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            const uint64_t stream_once = policy_evict_first(), reused = policy_evict_last();
-            mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
-            for (int dc = 0; dc < C::KD; ++dc)
-                tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
-                                 stream_once);
-            stamp(2);
-            int issued = 0;
-            for (int t = 0; t < n_tiles; ++t) {
+            const uint64_t reused = policy_evict_last();
+            int issued = 1;
+            for (int t = 1; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
-                const int nch = min(2, n_chunks - 2 * t);
                 stamp_tile(8, t);
-                mbar_expect_tx(bar(C::B_KF + st), nch * C::KD * BOX_BYTES);
-                for (int cc = 0; cc < nch; ++cc) {
-                    int back, u;
-                    bool sk;
-                    const int key0 = cw.key0(2 * t + cc, back, u, sk);
-                    for (int dc = 0; dc < C::KD; ++dc)
-                        tma_load_3d_hint(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
-                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st), reused);
-                }
+                issue_kv(&tmK, sK, C::B_KF, t, reused);
                 issued = t + 1;
             }
             if (*abort_flag) {  // let loads in flight land before the CTA leaves
@@ -391,17 +402,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
-                const int nch = min(2, n_chunks - 2 * t);
                 stamp_tile(24, t);
-                mbar_expect_tx(bar(C::B_VF + st), nch * C::KD * BOX_BYTES);
-                for (int cc = 0; cc < nch; ++cc) {
-                    int back, u;
-                    bool sk;
-                    const int key0 = cw.key0(2 * t + cc, back, u, sk);
-                    for (int dc = 0; dc < C::KD; ++dc)
-                        tma_load_3d_hint(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
-                                         dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st), reused);
-                }
+                issue_kv(&tmV, sV, C::B_VF, t, reused);
                 issued = t + 1;
             }
             if (*abort_flag) {
