@@ -17,7 +17,6 @@
 namespace pi {
 
 constexpr int kStatusOk = 0;
-constexpr int kStatusLaunch = -6;   // a kernel found its launch configuration unusable
 constexpr int kStatusTimeout = -7;
 
 constexpr float kLog2e = 1.4426950408889634f;
