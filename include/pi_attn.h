@@ -120,8 +120,10 @@ size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * pi_attn_bwd -- backward of pi_attn_fwd (the chain rule through the
  * definition above; bf16 tensors, fp32 accumulation).
  *   Inputs: q, k, v, alpha as for the forward; out [B,H,N,d] and lse [B,H,N]
- *   from pi_attn_fwd (out is validated but not read: D_i is recomputed from the
- *   probabilities); dout [B,H,N,d].
+ *   from pi_attn_fwd; dout [B,H,N,d].  D_i is recomputed exactly from the
+ *   probabilities; out only supplies dout_i . out_i, a per-row centre that keeps
+ *   the bf16 operands of the dq accumulation small (any out gives the same
+ *   result up to rounding).
  *   Outputs: dq [B,H,N,d], dk and dv [B,Hkv,N,d] (summed over the query heads
  *   of each KV group) bf16; dalpha [B,H,N] fp32 (may be NULL; zero in ECP mode),
  *   computed as dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)),

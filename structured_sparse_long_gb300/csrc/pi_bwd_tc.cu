@@ -4,16 +4,19 @@
 // Transformers for Efficient Long-Context Modeling", section 2.1-2.3; ECP page section 2):
 //   p_ij = exp(z_ij - lse_i),  dp_ij = dout_i . v_j,  D_i = sum_j p_ij dp_ij,
 //   dz_ij = p_ij (dp_ij - D_i),
-//   dq_i = tau sum_j dz_ij k_j = tau (sum_j (p dp)_ij k_j - D_i sum_j p_ij k_j),
+//   dq_i = tau sum_j dz_ij k_j = tau (sum_j p_ij (dp_ij - c_i) k_j - (D_i - c_i) sum_j p_ij k_j)
+//          for any per-row constant c_i,
 //   dk_j = tau sum_{h in group, i} dz_ij q_i,  dv_j = sum_{h in group, i} p_ij dout_i,
 //   dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)).
 //
 // Kernel 1 (query-major, one CTA per 128 query rows laid out as in the forward):
 //   per key tile, S = Q K^T and dP = dO V^T into TMEM; one thread per row forms p and p*dp,
-//   keeps D_i and the skip sums of dalpha in registers and writes p and p*dp (bf16) back to
-//   TMEM; two MMAs accumulate A1 = sum (p dp) K and A2 = sum p K.  The epilogue writes
-//   dq = tau (A1 - D A2), D_i (for kernel 2) and dalpha.  One sweep over the keys, and D_i
-//   is exact: it never goes through the bf16-rounded out.
+//   keeps D_i and the skip sums of dalpha in registers and writes p and p (dp - c) (bf16)
+//   back to TMEM; two MMAs accumulate A1 = sum p (dp - c) K and A2 = sum p K.  The epilogue
+//   writes dq = tau (A1 - (D - c) A2), D_i (for kernel 2) and dalpha.  One sweep over the
+//   keys, and D_i is exact: it never goes through the bf16-rounded out.  The centre c_i is
+//   dout_i . out_i from the bf16 out, within rounding of D_i, so that the bf16 operand of A1
+//   carries dz itself rather than p dp, whose cancellation against D A2 would cost accuracy.
 // Kernel 2 (key-major, one CTA per 128 keys of a KV head): for every 64-query chunk of every
 //   query head of the group whose band contains these keys, and every chunk of skip queries
 //   j + m*period: S^T = K Q^T and dP^T = V dO^T into TMEM; one thread per key forms p and dz
@@ -102,6 +105,7 @@ struct CfgQ {
 };
 
 struct DqArgs {
+    const __nv_bfloat16 *out, *dout;  // rows of the forward output and its gradient (centre c_i)
     const float *alpha;
     const float *lse;
     float *Dws;
@@ -317,6 +321,24 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         float dsum = 0.f, skip_p = 0.f, skip_pdp = 0.f;
         bool any_skip = false;
         bool ok = true;
+        // centre c_i = dout_i . out_i (bf16 rows); D_i itself is accumulated exactly below
+        float cen = 0.f;
+        if (live) {
+            const __nv_bfloat16 *orow = args.out + row_g * D, *grow = args.dout + row_g * D;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < D; c += 8) {
+                float o8[8], g8[8];
+                load8(orow + c, o8);
+                load8(grow + c, g8);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    acc0 = fmaf(o8[e], g8[e], acc0);
+                    acc1 = fmaf(o8[e + 1], g8[e + 1], acc1);
+                }
+            }
+            cen = acc0 + acc1;
+        }
 
         for (int t = 0; t < n_tiles; ++t) {
             ok = wait_bar(bar(C::B_SF), t & 1, wc);
@@ -365,9 +387,9 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                             skip_pdp += w0 + w1;
                         }
                         pp[c / 2] = pack_bf16(p0v, p1v);
-                        pw[c / 2] = pack_bf16(w0, w1);
+                        pw[c / 2] = pack_bf16(fmaf(-p0v, cen, w0), fmaf(-p1v, cen, w1));
                     }
-                    // A1 operand (p*dp) over the S columns, A2 operand (p) over the dP columns;
+                    // A1 operand p (dp - c) over the S columns, A2 operand p over the dP columns;
                     // both chunk halves' values are already in registers
                     tmem_st8(tbase + lane_base + C::S_COL + cc * (CHUNK / 2) + half * 8, pw);
                     tmem_st8(tbase + lane_base + C::DP_COL + cc * (CHUNK / 2) + half * 8, pp);
@@ -378,12 +400,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             mbar_arrive(bar(C::B_PR));
         }
 
-        // ---- epilogue: dq = tau (A1 - D A2) -> bf16 -> shared (Q buffer) -> TMA store
+        // ---- epilogue: dq = tau (A1 - (D - c) A2) -> bf16 -> shared (Q buffer) -> TMA store
         if (ok) {
             ok = wait_bar(bar(C::B_AF), 0, wc);
             ok = __all_sync(0xffffffffu, ok);
         }
         const float tau = s.scale_log2 / kLog2e;
+        const float dres = dsum - cen;
         if (ok) {
             tc_fence_after();
             __syncwarp();
@@ -396,8 +419,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 uint32_t pk[8];
 #pragma unroll
                 for (int c = 0; c < 16; c += 2) {
-                    const float x0 = tau * (__uint_as_float(a1[c]) - dsum * __uint_as_float(a2[c]));
-                    const float x1 = tau * (__uint_as_float(a1[c + 1]) - dsum * __uint_as_float(a2[c + 1]));
+                    const float x0 = tau * fmaf(-dres, __uint_as_float(a2[c]), __uint_as_float(a1[c]));
+                    const float x1 = tau * fmaf(-dres, __uint_as_float(a2[c + 1]), __uint_as_float(a1[c + 1]));
                     pk[c / 2] = pack_bf16(x0, x1);
                 }
                 const int dc = oc >> 2, quarter = oc & 3;
@@ -853,7 +876,8 @@ cudaError_t launch_bwd_dq_tc(const LaunchBwd &L, int *status, uint64_t timeout_n
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
-    DqArgs a{L.alpha, L.lse, L.Dws, L.dalpha, s, GP, status, timeout_ns};
+    DqArgs a{static_cast<const __nv_bfloat16 *>(L.out), static_cast<const __nv_bfloat16 *>(L.dout), L.alpha,
+             L.lse, L.Dws, L.dalpha, s, GP, status, timeout_ns};
     const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (s.d == 64) return launch_dq<64>(mq, mg, mk, mv, mdq, a, (unsigned)grid, st);

@@ -244,6 +244,26 @@ def test_small_backward(spec):
     assert_close("dalpha", dal.cpu().numpy(), ral, dt)
 
 
+def test_backward_dq_precision_d128_gqa():
+    """A d=128 GQA case (seed 1) whose dq lost accuracy when the bf16 operand of the dq
+    accumulation carried p*dp and D*sum(p k) was subtracted afterwards; centring the operand
+    on dout.out keeps dq within the bf16 bound."""
+    w = small_case("bwd-dq-d128", 1, 8, 2, 300, 128, 64, 96, 3, MODE_PI, "bf16", seed=1,
+                   backward=True)
+    inp = make_inputs(w, with_dout=True)
+    dev = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    out, lse = pa.fwd(dev["q"], dev["k"], dev["v"], dev["alpha"], w.k_local, w.period, w.S, w.mode)
+    dq, dk, dv, dal = pa.bwd(dev["q"], dev["k"], dev["v"], dev["alpha"], out, lse, dev["dout"],
+                             w.k_local, w.period, w.S, w.mode)
+    torch.cuda.synchronize()
+    assert pa.status() == 0
+    rq, rk, rv, ral = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["dout"], w.k_local,
+                                 w.period, w.S, w.mode)
+    assert_close("dq", dq.float().cpu().numpy(), rq, "bf16")
+    assert_close("dk", dk.float().cpu().numpy(), rk, "bf16")
+    assert_close("dv", dv.float().cpu().numpy(), rv, "bf16")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     pa.debug_wait_timeout(2000)  # 2 ms on a barrier nothing completes
     assert pa.status() == -7
