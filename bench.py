@@ -86,24 +86,31 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha() -> str:
+KERNEL_SOURCES = {
+    "fwd": ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"),
+    "bwd": ("pi_bwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"),
+}
+
+
+def kernel_source_sha(kind: str = "fwd") -> str:
     h = hashlib.sha256()
-    for name in ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "structured_sparse_long_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the forward kernel from a committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(PROFILE_DIR, f"pi_fwd_tc_{workload}.md")
+def profiled_traffic(workload: str, kind: str = "fwd"):
+    """DRAM bytes of one forward launch (kind "fwd") or of one backward call, both of its
+    kernels (kind "bwd"), from a committed ncu summary -- if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"pi_{kind}_tc_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha():
+    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha(kind):
         return None
     return float(m_b.group(1))
 
@@ -356,7 +363,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         achieved, peak, unit = dom_bytes / (dom_ms / 1e3) / 1e9, hbm, "GB/s"
     else:
         achieved, peak, unit = dom_flops / (dom_ms / 1e3) / 1e12, tensor, "TFLOP/s"
-    traffic = profiled_traffic(w.name) if dom == "pi_attn_fwd" else None
+    traffic = profiled_traffic(w.name, "fwd" if dom == "pi_attn_fwd" else "bwd")
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                 "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}, burst)",
