@@ -32,7 +32,7 @@ _lock = threading.Lock()
 _lib = None
 
 DT_F64, DT_F32, DT_BF16 = 0, 1, 2
-MODE_PI, MODE_ECP = 0, 1
+MODE_PI, MODE_ECP, MODE_PI_BIDIR = 0, 1, 2
 
 
 def build(force: bool = False) -> str:

@@ -19,6 +19,9 @@
  *     - 2.3 adaptive fusion: one softmax over the union of local and skip
  *       neighbours, with the per-token, per-head gate alpha entering as a
  *       log-prior: +ln(alpha) on local logits, +ln(1-alpha) on skip logits.
+ *   Bidirectional pi-Attention (same page, 2.1 and 2.2 in their general,
+ *   non-causal form): the band is i-k .. i+k and the skip keys are i - m*pi and
+ *   i + m*pi, each clipped to [0, N); the priors are those of the causal form.
  *   ECP ("Efficient Context Propagating Perceiver Architectures for
  *   Auto-Regressive Language Modeling", section 2, paired-segment PAR block):
  *     queries of half-segment s = floor(i/c) attend causally to keys of
@@ -52,6 +55,7 @@
 
 #define MODE_PI 0
 #define MODE_ECP 1
+#define MODE_PI_BIDIR 2
 
 static double ld(const void *p, int dt, size_t idx) {
     if (dt == DT_F64) return ((const double *)p)[idx];
@@ -64,15 +68,28 @@ static double ld(const void *p, int dt, size_t idx) {
 
 /* Upper bound on the neighbour count of one query row. */
 static long max_neighbours(long N, int mode, long k_local, int S) {
-    long n = (mode == MODE_PI) ? (k_local + 1 + S) : (2 * k_local + 1);
-    return n < N + S + 1 ? n : N + S + 1;
+    long n = (mode == MODE_PI) ? (k_local + 1 + S)
+             : (mode == MODE_PI_BIDIR) ? (2 * k_local + 1 + 2 * (long)S) : (2 * k_local + 1);
+    return n < N + 2 * (long)S + 1 ? n : N + 2 * (long)S + 1;
 }
 
-/* Neighbour list of query i: keys in idx[], tag 0 = local, 1 = skip. */
-static long neighbours(long i, int mode, long k_local, long period, int S,
+/* Neighbour list of query i (sequence length N): keys in idx[], tag 0 = local, 1 = skip. */
+static long neighbours(long i, long N, int mode, long k_local, long period, int S,
                        long *idx, int *tag) {
-    long n = 0, lo, j;
-    if (mode == MODE_PI) {
+    long n = 0, lo, hi, j;
+    if (mode == MODE_PI_BIDIR) {
+        lo = i - k_local;
+        if (lo < 0) lo = 0;
+        hi = i + k_local;
+        if (hi > N - 1) hi = N - 1;
+        for (j = lo; j <= hi; ++j) { idx[n] = j; tag[n] = 0; ++n; }
+        for (int m = 1; m <= S; ++m) {
+            long off = (long)m * period;
+            if (off <= k_local) continue;    /* inside the band already */
+            if (i - off >= 0) { idx[n] = i - off; tag[n] = 1; ++n; }
+            if (i + off < N) { idx[n] = i + off; tag[n] = 1; ++n; }
+        }
+    } else if (mode == MODE_PI) {
         lo = i - k_local;
         if (lo < 0) lo = 0;
         for (j = lo; j <= i; ++j) { idx[n] = j; tag[n] = 0; ++n; }
@@ -102,7 +119,7 @@ void oracle_counts(long N, int mode, long k_local, long period, int S,
         int *tag = (int *)malloc(sizeof(int) * cap);
 #pragma omp for schedule(static)
         for (long i = 0; i < N; ++i) {
-            long n = neighbours(i, mode, k_local, period, S, idx, tag);
+            long n = neighbours(i, N, mode, k_local, period, S, idx, tag);
             long long s = 0;
             for (long t = 0; t < n; ++t) s += idx[t];
             count[i] = n;
@@ -128,7 +145,7 @@ static double one_row(const double *q, const double *k, const double *v, const f
         double dot = 0.0;
         for (long c = 0; c < d; ++c) dot += qrow[c] * krow[c];
         double prior = 0.0;
-        if (mode == MODE_PI) prior = (tag[t] == 0) ? log(a) : log1p(-a);
+        if (mode != MODE_ECP) prior = (tag[t] == 0) ? log(a) : log1p(-a);
         z[t] = dot * scale + prior;
         if (z[t] > M) M = z[t];
     }
@@ -168,7 +185,7 @@ int oracle_fwd(const void *q, const void *k, const void *v, int dt, const float 
                int mode, long i_begin, long i_end, double *out, double *lse, double *P) {
     if (B <= 0 || H <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || H % Hkv != 0) return -1;
     if (mode == MODE_ECP && k_local <= 0) return -1;
-    if (mode == MODE_PI && S > 0 && period <= 0) return -1;
+    if (mode != MODE_ECP && S > 0 && period <= 0) return -1;
     if (i_begin < 0 || i_end > N || i_begin > i_end) return -1;
     if (P && (i_begin != 0 || i_end != N)) return -1;
     long rows = i_end - i_begin;
@@ -189,7 +206,7 @@ int oracle_fwd(const void *q, const void *k, const void *v, int dt, const float 
             long b = r / (H * rows);
             long h = (r / rows) % H;
             long i = i_begin + r % rows;
-            long n = neighbours(i, mode, k_local, period, S, idx, tag);
+            long n = neighbours(i, N, mode, k_local, period, S, idx, tag);
             double *orow = out + (size_t)r * d;
             lse[r] = one_row(qd, kd, vd, alpha, H, Hkv, N, d, mode, b, h, i, n, idx, tag, z, p,
                              orow);
@@ -216,7 +233,7 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
                double *dalpha) {
     if (B <= 0 || H <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || H % Hkv != 0) return -1;
     if (mode == MODE_ECP && k_local <= 0) return -1;
-    if (mode == MODE_PI && S > 0 && period <= 0) return -1;
+    if (mode != MODE_ECP && S > 0 && period <= 0) return -1;
     long G = H / Hkv;
     long cap = max_neighbours(N, mode, k_local, S);
     double scale = 1.0 / sqrt((double)d);
@@ -243,7 +260,7 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
             const double *vg = vd + (size_t)bg * N * d;
             for (long h = g * G; h < (g + 1) * G; ++h) {
                 for (long i = 0; i < N; ++i) {
-                    long n = neighbours(i, mode, k_local, period, S, idx, tag);
+                    long n = neighbours(i, N, mode, k_local, period, S, idx, tag);
                     one_row(qd, kd, vd, alpha, H, Hkv, N, d, mode, b, h, i, n, idx, tag, z, p, orow);
                     size_t qoff = (((size_t)b * H + h) * N + i) * d;
                     const double *qrow = qd + qoff;
@@ -267,7 +284,7 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
                     }
                     if (dalpha) {
                         double g_a = 0.0;
-                        if (mode == MODE_PI) {
+                        if (mode != MODE_ECP) {
                             double a = alpha ? (double)alpha[((size_t)b * H + h) * N + i] : 1.0;
                             g_a = sum_local / a - sum_skip / (1.0 - a);
                             if (sum_skip == 0.0) g_a = sum_local / a;

@@ -15,7 +15,8 @@ import torch
 
 
 def union_masks(N, k_local, period, S, mode):
-    """(local, skip) boolean [N, N] masks; for ECP skip is all False."""
+    """(local, skip) boolean [N, N] masks; for ECP skip is all False.  Mode 2 is the
+    bidirectional form of the band and skips (same page, 2.1 and 2.2)."""
     i = torch.arange(N).view(N, 1)
     j = torch.arange(N).view(1, N)
     diff = i - j
@@ -25,6 +26,12 @@ def union_masks(N, k_local, period, S, mode):
         for m in range(1, S + 1):
             if m * period > k_local:
                 skip |= diff == m * period
+    elif mode == 2:  # bidirectional: |i - j| <= k, skips at i -/+ m*period
+        local = diff.abs() <= k_local
+        skip = torch.zeros(N, N, dtype=torch.bool)
+        for m in range(1, S + 1):
+            if m * period > k_local:
+                skip |= diff.abs() == m * period
     else:
         c = k_local
         local = (diff >= 0) & ((j // c) >= (i // c) - 1)
@@ -45,7 +52,7 @@ def dense_forward(q, k, v, alpha, k_local, period, S, mode):
     local, skip = union_masks(N, k_local, period, S, mode)
     scores = torch.matmul(q, kk.transpose(-1, -2)) / math.sqrt(d)
     neg_inf = torch.tensor(float("-inf"), dtype=q.dtype)
-    if mode == 0:
+    if mode in (0, 2):
         a = alpha.to(q.dtype).unsqueeze(-1) if alpha is not None else torch.ones(B, H, N, 1,
                                                                                 dtype=q.dtype)
         bias = torch.where(local, torch.log(a), torch.where(skip, torch.log1p(-a), neg_inf))
