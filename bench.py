@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from structured_sparse_long_gb300.synth import MODE_ECP, WORKLOADS, make_inputs  # noqa: E402
+from structured_sparse_long_gb300.synth import MODE_ECP, MODE_PI_BIDIR, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "sparse-attn tokens/s and useful TFLOP/s at N=4K–64K; % of roofline (1×GB300)"
 L2_BYTES = 129 * 1024 * 1024
@@ -55,6 +55,11 @@ def pairs_per_head(N, k, period, S, mode) -> int:
             total += n * (n + 1) // 2 if s == 0 else n * (c + 1) + n * (n - 1) // 2
             s += 1
         return total
+    if mode == MODE_PI_BIDIR:  # |i - j| <= k, and skips on both sides
+        kk = min(k, N - 1)
+        band = N + 2 * (kk * N - kk * (kk + 1) // 2)
+        skip = sum(2 * max(0, N - m * period) for m in range(1, S + 1) if m * period > k)
+        return band + skip
     band = N * (k + 1) - k * (k + 1) // 2 if k < N else N * (N + 1) // 2
     skip = sum(max(0, N - m * period) for m in range(1, S + 1) if m * period > k)
     return band + skip

@@ -6,7 +6,7 @@ script, a thin ctypes binding with the same names as the C entry points, and
 the seeded synthetic input generators.  Importing the package loads nothing;
 the first call loads the library and fails loudly if it is missing.
 """
-from ._binding import (MODE_ECP, MODE_PI, PiAttnError, bwd, bwd_noalloc,  # noqa: F401
+from ._binding import (MODE_ECP, MODE_PI, MODE_PI_BIDIR, PiAttnError, bwd, bwd_noalloc,  # noqa: F401
                        bwd_workspace_size,
                        debug_counts, debug_probs, debug_trace, debug_wait_timeout, fwd, lib_path,
                        load,
@@ -14,4 +14,4 @@ from ._binding import (MODE_ECP, MODE_PI, PiAttnError, bwd, bwd_noalloc,  # noqa
 
 __all__ = ["fwd", "bwd", "bwd_noalloc", "bwd_workspace_size", "status", "strerror", "debug_counts",
            "debug_probs", "debug_trace", "debug_wait_timeout", "load", "lib_path", "PiAttnError",
-           "MODE_PI", "MODE_ECP"]
+           "MODE_PI", "MODE_ECP", "MODE_PI_BIDIR"]

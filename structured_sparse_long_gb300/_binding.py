@@ -20,6 +20,7 @@ from . import build as _build
 
 MODE_PI = 0
 MODE_ECP = 1
+MODE_PI_BIDIR = 2  # bidirectional band and skips (forward only)
 PI_OK = 0
 
 _lock = threading.Lock()

@@ -33,11 +33,11 @@ int *status_word() {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int validate_shape(int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode) {
-    if (mode != PI_MODE_PI && mode != PI_MODE_ECP) return PI_ERR_UNSUPPORTED;
+    if (mode != PI_MODE_PI && mode != PI_MODE_ECP && mode != PI_MODE_PI_BIDIR) return PI_ERR_UNSUPPORTED;
     if (B <= 0 || H <= 0 || Hkv <= 0 || N <= 0) return PI_ERR_SHAPE;
     if (H % Hkv != 0) return PI_ERR_SHAPE;
     if (k_local < 0 || S < 0) return PI_ERR_SHAPE;
-    if (mode == PI_MODE_PI && S > 0 && period <= 0) return PI_ERR_SHAPE;
+    if (mode != PI_MODE_ECP && S > 0 && period <= 0) return PI_ERR_SHAPE;
     if (mode == PI_MODE_ECP && (k_local <= 0 || S != 0)) return PI_ERR_SHAPE;
     if (d != 32 && d != 64 && d != 128) return PI_ERR_UNSUPPORTED;
     const long long rows = (long long)B * H * N;
@@ -49,7 +49,7 @@ int validate_fwd(const void *q, const void *k, const void *v, const float *alpha
                  int Hkv, int N, int d, int k_local, int period, int S, int mode, const void *out,
                  const float *lse) {
     if (!q || !k || !v || !out || !lse) return PI_ERR_NULL;
-    if (mode == PI_MODE_PI && !alpha) return PI_ERR_NULL;
+    if (mode != PI_MODE_ECP && !alpha) return PI_ERR_NULL;
     const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     if (rc != PI_OK) return rc;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return PI_ERR_ALIGN;
@@ -60,7 +60,7 @@ int validate_fwd(const void *q, const void *k, const void *v, const float *alpha
 pi::Shape make_shape(int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode) {
     pi::Shape s;
     s.B = B; s.H = H; s.Hkv = Hkv; s.N = N; s.d = d;
-    s.k_local = k_local; s.period = period; s.S = (mode == PI_MODE_PI) ? S : 0; s.mode = mode;
+    s.k_local = k_local; s.period = period; s.S = (mode != PI_MODE_ECP) ? S : 0; s.mode = mode;
     s.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     return s;
 }
@@ -75,7 +75,7 @@ int run_fwd(const void *q, const void *k, const void *v, const float *alpha, int
     int *status = status_word();
     if (!status) return PI_ERR_CUDA;
     pi::LaunchFwd L;
-    L.q = q; L.k = k; L.v = v; L.alpha = (mode == PI_MODE_PI) ? alpha : nullptr;
+    L.q = q; L.k = k; L.v = v; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
     L.out = out; L.lse = lse;
     L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     L.fp32 = fp32; L.dbg = dbg; L.cnt = cnt; L.isum = isum; L.lse_in = lse_in; L.P = P;
@@ -91,9 +91,10 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
             int period, int S, int mode, void *dq, void *dk, void *dv, float *dalpha, void *workspace,
             size_t workspace_bytes, void *stream, bool fp32) {
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return PI_ERR_NULL;
-    if (mode == PI_MODE_PI && !alpha) return PI_ERR_NULL;
+    if (mode != PI_MODE_ECP && !alpha) return PI_ERR_NULL;
     const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     if (rc != PI_OK) return rc;
+    if (mode == PI_MODE_PI_BIDIR) return PI_ERR_UNSUPPORTED;  // the backward is causal/ECP only
     const void *p16[] = {q, k, v, out, dout, dq, dk, dv};
     for (const void *p : p16)
         if (!aligned(p, 16)) return PI_ERR_ALIGN;
@@ -103,7 +104,7 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
     if (!workspace || workspace_bytes < need) return PI_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PI_ERR_ALIGN;
     pi::LaunchBwd L;
-    L.q = q; L.k = k; L.v = v; L.alpha = (mode == PI_MODE_PI) ? alpha : nullptr;
+    L.q = q; L.k = k; L.v = v; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
     L.out = out; L.lse = lse; L.dout = dout; L.dq = dq; L.dk = dk; L.dv = dv; L.dalpha = dalpha;
     L.Dws = static_cast<float *>(workspace);
     L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
@@ -257,7 +258,7 @@ int pi_attn_debug_trace(const void *q, const void *k, const void *v, const float
     int *status = status_word();
     if (!status) return PI_ERR_CUDA;
     pi::LaunchFwd L;
-    L.q = q; L.k = k; L.v = v; L.alpha = (mode == PI_MODE_PI) ? alpha : nullptr;
+    L.q = q; L.k = k; L.v = v; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
     L.out = out; L.lse = lse;
     L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     L.fp32 = false; L.dbg = 3; L.cnt = nullptr; L.isum = nullptr; L.lse_in = nullptr; L.P = nullptr;

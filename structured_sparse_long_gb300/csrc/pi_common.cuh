@@ -6,6 +6,9 @@
 //            Long-Context Modeling", section 2.1 and 2.2):
 //            band  [max(0, i - k_local), i]
 //            skip  i - m*period for m = 1..S when m*period > k_local and >= 0
+//   bidirectional pi mode (same page, 2.1 and 2.2 in their general form):
+//            band  [max(0, i - k_local), min(N - 1, i + k_local)]
+//            skip  i -/+ m*period for m = 1..S when m*period > k_local, inside [0, N)
 //   ECP mode ("Efficient Context Propagating Perceiver Architectures...",
 //            section 2, PAR block): [max(0, (floor(i/c) - 1) * c), i], c = k_local
 #pragma once
@@ -28,14 +31,17 @@ struct Shape {
     int k_local;       // band width k (pi) or half-segment length c (ECP)
     int period;        // skip stride (pi mode)
     int S;             // skip multiples (pi mode)
-    int mode;          // 0 = pi, 1 = ECP
+    int mode;          // 0 = pi (causal), 1 = ECP, 2 = pi (bidirectional)
     float scale_log2;  // log2(e) / sqrt(d): raw score -> log2-domain logit
 };
+
+constexpr int kModeEcp = 1;
+constexpr int kModeBidir = 2;
 
 // First band key of query i.
 __host__ __device__ __forceinline__ int band_lo(int i, int mode, int k_local) {
     int lo;
-    if (mode == 0) {
+    if (mode != kModeEcp) {
         lo = i - k_local;
     } else {
         lo = (i / k_local - 1) * k_local;
@@ -43,10 +49,17 @@ __host__ __device__ __forceinline__ int band_lo(int i, int mode, int k_local) {
     return lo < 0 ? 0 : lo;
 }
 
+// Last band key of query i.
+__host__ __device__ __forceinline__ int band_hi(int i, int N, int mode, int k_local) {
+    if (mode != kModeBidir) return i;
+    const long long hi = (long long)i + k_local;
+    return hi > N - 1 ? N - 1 : (int)hi;
+}
+
 // Last query position whose band contains key j (for key-major passes).
 __host__ __device__ __forceinline__ int band_last_query(int j, int N, int mode, int k_local) {
     long long hi;
-    if (mode == 0) {
+    if (mode != kModeEcp) {
         hi = (long long)j + k_local;
     } else {
         hi = ((long long)(j / k_local) + 2) * k_local - 1;

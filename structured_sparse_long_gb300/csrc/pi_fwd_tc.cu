@@ -216,17 +216,20 @@ constexpr int kTraceTiles = 16;
 
 // Key chunk ci of the block: first key position, whether it is a skip chunk,
 // its skip distance m*period and sub-block index u.
+// Skip blocks come after the band: first the n_back blocks of keys i - m*period, then (in the
+// bidirectional mode) those of keys i + m*period, both for m = m_first, m_first + 1, ...;
+// `back` is the signed distance i - key.
 struct ChunkWalk {
-    int lo0, n_band, m_first, cpb, cpb_log2, p0, period;
+    int lo0, n_band, m_first, cpb, cpb_log2, p0, period, n_back;
     __device__ __forceinline__ int key0(int ci, int &back, int &u, bool &skip) const {
         if (ci < n_band) {
             back = 0; u = 0; skip = false;
             return lo0 + ci * CHUNK;
         }
         const int sc = ci - n_band;  // cpb = R / 32 is 1, 2 or 4
-        const int m = m_first + (sc >> cpb_log2);
+        const int blk = sc >> cpb_log2;
         u = sc & (cpb - 1);
-        back = m * period;
+        back = (blk < n_back) ? (m_first + blk) * period : -(m_first + blk - n_back) * period;
         skip = true;
         return p0 - back + u * CHUNK;
     }
@@ -294,13 +297,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     cw.cpb = R / CHUNK;
     cw.cpb_log2 = (cw.cpb == 4) ? 2 : (cw.cpb == 2) ? 1 : 0;
     cw.lo0 = band_lo(p0, s.mode, s.k_local);
-    const int band_hi = min(s.N - 1, p0 + R - 1);
-    cw.n_band = (band_hi - cw.lo0) / CHUNK + 1;
+    const int blk_hi = band_hi(min(s.N - 1, p0 + R - 1), s.N, s.mode, s.k_local);
+    cw.n_band = (blk_hi - cw.lo0) / CHUNK + 1;
     int n_skip_blocks = 0;
     cw.m_first = args.m_first;
-    if (s.mode == 0 && s.S > 0) {
-        const int m_last = min(s.S, (p0 + R - 1) / s.period);
-        n_skip_blocks = max(0, m_last - cw.m_first + 1);
+    cw.n_back = 0;
+    if (s.mode != kModeEcp && s.S > 0) {
+        const int m_last = min(s.S, (p0 + R - 1) / s.period);  // some row has i - m*period >= 0
+        cw.n_back = max(0, m_last - cw.m_first + 1);
+        n_skip_blocks = cw.n_back;
+        if (s.mode == kModeBidir) {
+            const int m_last_f = min(s.S, (s.N - 1 - p0) / s.period);  // some row has i + m*period < N
+            n_skip_blocks += max(0, m_last_f - cw.m_first + 1);
+        }
     }
     const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
     const int n_tiles = (n_chunks + 1) / 2;
@@ -311,7 +320,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (p0 + R <= s.N) {
         const int lo_last = band_lo(p0 + R - 1, s.mode, s.k_local);
         full_lo = (lo_last - cw.lo0 + CHUNK - 1) / CHUNK;
-        const int span = p0 - (CHUNK - 1) - cw.lo0;
+        const int span = band_hi(p0, s.N, s.mode, s.k_local) - (CHUNK - 1) - cw.lo0;
         full_hi = span >= 0 ? min(span / CHUNK, cw.n_band - 1) : -1;
     }
 
@@ -485,9 +494,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const bool row_ok = i < s.N;
         const long long row_g = ((long long)b * s.H + h) * s.N + i;
         const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
-        const float off_band = (s.mode == 0) ? log2f(al) : 0.f;
+        const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
         const float off_skip = log2f(1.f - al);
         const int lo_i = band_lo(i, s.mode, s.k_local);
+        const int hi_i = band_hi(i, s.N, s.mode, s.k_local);
         const float sc = s.scale_log2;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         float lse2_in = 0.f;
@@ -503,12 +513,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             key0 = cw.key0(ci, back, u, sk);
             if (!sk) {
                 clo = max(lo_i - key0, 0);
-                chi = min(i - key0, CHUNK - 1);
+                chi = min(hi_i - key0, CHUNK - 1);
                 off = off_band;
             } else {
                 const int jk = i - back;
                 const int c = jk - key0;
-                if (jk >= 0 && c >= 0 && c < CHUNK) { clo = c; chi = c; }
+                if (jk >= 0 && jk < s.N && c >= 0 && c < CHUNK) { clo = c; chi = c; }
                 else { clo = CHUNK; chi = -1; }
                 off = off_skip;
             }
@@ -750,7 +760,7 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
     int m_first = 1;
-    if (s.mode == 0 && s.S > 0) m_first = s.k_local / s.period + 1;  // smallest m with m*period > k
+    if (s.mode != kModeEcp && s.S > 0) m_first = s.k_local / s.period + 1;  // smallest m with m*period > k
     TcArgs a{L.alpha, L.lse, s, GP, m_first, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P,
              L.trace, L.n_trace};
     if (s.H / GP > 65535 || s.B > 65535) return cudaErrorInvalidConfiguration;

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(FwdArgs a, Shape s) {
     __syncwarp();
 
     const float al = a.alpha ? a.alpha[row] : 1.f;
-    const float off_b = (s.mode == 0) ? log2f(al) : 0.f;
+    const float off_b = (s.mode != kModeEcp) ? log2f(al) : 0.f;
     const float off_s = log2f(1.f - al);
     constexpr int RC = D / 32;
     float o[RC];
@@ -123,18 +123,20 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(FwdArgs a, Shape s) {
         m = mn;
     };
 
-    const int lo = band_lo(i, s.mode, s.k_local);
-    for (int j0 = lo; j0 <= i; j0 += 32) {
+    const int lo = band_lo(i, s.mode, s.k_local), hi = band_hi(i, s.N, s.mode, s.k_local);
+    for (int j0 = lo; j0 <= hi; j0 += 32) {
         const int j = j0 + lane;
-        chunk(j, j <= i, off_b);
+        chunk(j, j <= hi, off_b);
     }
-    if (s.mode == 0) {
-        for (int m0 = 1; m0 <= s.S; m0 += 32) {
-            const int mm = m0 + lane;
-            const long long back = (long long)mm * s.period;
-            const long long jj = (long long)i - back;
-            const bool valid = mm <= s.S && back > s.k_local && jj >= 0;
-            chunk(valid ? (int)jj : 0, valid, off_s);
+    if (s.mode != kModeEcp) {
+        for (int dir = -1; dir <= ((s.mode == kModeBidir) ? 1 : -1); dir += 2) {  // i - m pi, i + m pi
+            for (int m0 = 1; m0 <= s.S; m0 += 32) {
+                const int mm = m0 + lane;
+                const long long off = (long long)mm * s.period;
+                const long long jj = (long long)i + dir * off;
+                const bool valid = mm <= s.S && off > s.k_local && jj >= 0 && jj < s.N;
+                chunk(valid ? (int)jj : 0, valid, off_s);
+            }
         }
     }
 

@@ -12,6 +12,8 @@ Context Propagating Perceiver Architectures...", section 2, PAR block):
   C3  ECP paired-segment bf16 fwd B2 H16 Hkv16 N8192  d64  c512 (no skip)
   C4  long-context GQA bf16 fwd   B1 H16 Hkv4  N65536 d128 k256 pi1024 S4
   C5  training fwd+bwd bf16       B2 H16 Hkv16 N16384 d64  k256 pi512  S2
+  C6  bidirectional GQA bf16 fwd  B1 H16 Hkv4  N65536 d128 k256 pi1024 S4 (band i-k..i+k,
+                                  skips i -/+ m*pi: the general form of the same page, 2.1-2.2)
 
 Draw order per workload: q, k, v, alpha, dout, from one CPU torch.Generator
 seeded with the workload's seed.  Values are drawn in fp32 and then cast to
@@ -27,6 +29,7 @@ import torch
 
 MODE_PI = 0
 MODE_ECP = 1
+MODE_PI_BIDIR = 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -40,7 +43,7 @@ class Workload:
     k_local: int          # band width k (pi mode) or half-segment length c (ECP mode)
     period: int           # skip period pi (pi mode), unused in ECP mode
     S: int                # number of skip multiples, 0 in ECP mode
-    mode: int             # MODE_PI or MODE_ECP
+    mode: int             # MODE_PI, MODE_ECP or MODE_PI_BIDIR
     dtype: str            # "f32" or "bf16"
     seed: int
     qkv_scale: str        # "unit": N(0,1); "inv_sqrt_d": N(0,1)/sqrt(d)
@@ -71,6 +74,9 @@ WORKLOADS = {
     "C5": Workload("C5", 2, 16, 16, 16384, 64, 256, 512, 2, MODE_PI, "bf16", 4, "unit",
                    "sigmoid(1.0)", backward=True,
                    description="training fwd+bwd bf16 pi-Attention"),
+    "C6": Workload("C6", 1, 16, 4, 65536, 128, 256, 1024, 4, MODE_PI_BIDIR, "bf16", 5, "unit",
+                   "sigmoid(1.5)",
+                   description="long-context GQA bf16 bidirectional pi-Attention fwd"),
 }
 
 

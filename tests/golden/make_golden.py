@@ -1,10 +1,11 @@
 """Writes tests/golden/pair_counts.json using only the oracle (oracle.counts).
 
-The per-(b, h) attended-pair totals and key-index sums of the five workloads.
+The per-(b, h) attended-pair totals and key-index sums of the six workloads.
 Neighbour sets: "pi-Attention: Periodic Sparse Transformers for Efficient
 Long-Context Modeling" section 2.1 (causal band [i-k, i]) and 2.2 (skip keys
 i - m*pi, m = 1..S, kept when m*pi > k and i - m*pi >= 0); ECP page section 2
-(keys of half-segments s-1 and s, causal).
+(keys of half-segments s-1 and s, causal); bidirectional pi-Attention, the general form of
+2.1-2.2 (band [i-k, i+k] and skip keys i -/+ m*pi inside [0, N)).
 
 Run:  python tests/golden/make_golden.py
 """
@@ -23,6 +24,7 @@ WORKLOADS = {
     "C3": dict(N=8192, k_local=512, period=0, S=0, mode=1),
     "C4": dict(N=65536, k_local=256, period=1024, S=4, mode=0),
     "C5": dict(N=16384, k_local=256, period=512, S=2, mode=0),
+    "C6": dict(N=65536, k_local=256, period=1024, S=4, mode=2),
 }
 
 

@@ -80,7 +80,9 @@ def test_fwd_validation(lib, fn):
     assert fwd_call(lib, mode=1, kl=16, S=1, fn=fn) == PI_ERR_SHAPE               # ECP has no skip
     assert fwd_call(lib, d=48, fn=fn) == PI_ERR_UNSUPPORTED
     assert fwd_call(lib, d=256, fn=fn) == PI_ERR_UNSUPPORTED
-    assert fwd_call(lib, mode=2, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, mode=3, fn=fn) == PI_ERR_UNSUPPORTED
+    assert fwd_call(lib, mode=2, alpha=None, fn=fn) == PI_ERR_NULL   # bidirectional needs alpha
+    assert fwd_call(lib, mode=2, per=0, S=2, fn=fn) == PI_ERR_SHAPE
     assert fwd_call(lib, B=1 << 12, H=1 << 10, Hkv=1 << 10, N=1 << 10, fn=fn) == PI_ERR_UNSUPPORTED
     assert fwd_call(lib, q=A16 + 8, fn=fn) == PI_ERR_ALIGN
     assert fwd_call(lib, v=A16 + 2, fn=fn) == PI_ERR_ALIGN
@@ -88,8 +90,9 @@ def test_fwd_validation(lib, fn):
     assert fwd_call(lib, lse=A16 + 2, fn=fn) == PI_ERR_ALIGN
 
 
-def bwd_call(lib, ws=A16, ws_bytes=1 << 20, dq=A16, alpha=A16, d=64, dalpha=A16, N=64, fn="pi_attn_bwd"):
-    return getattr(lib, fn)(A16, A16, A16, alpha, A16, A16, A16, 1, 2, 2, N, d, 8, 16, 1, 0,
+def bwd_call(lib, ws=A16, ws_bytes=1 << 20, dq=A16, alpha=A16, d=64, dalpha=A16, N=64, mode=0,
+             fn="pi_attn_bwd"):
+    return getattr(lib, fn)(A16, A16, A16, alpha, A16, A16, A16, 1, 2, 2, N, d, 8, 16, 1, mode,
                             dq, A16, A16, dalpha, ws, ws_bytes, None)
 
 
@@ -102,6 +105,7 @@ def test_bwd_validation(lib, fn):
     assert bwd_call(lib, dalpha=A16 + 1, fn=fn) == PI_ERR_ALIGN
     assert bwd_call(lib, ws=None, fn=fn) == PI_ERR_WORKSPACE
     assert bwd_call(lib, ws_bytes=16, fn=fn) == PI_ERR_WORKSPACE
+    assert bwd_call(lib, mode=2, fn=fn) == PI_ERR_UNSUPPORTED  # the backward is causal/ECP only
 
 
 def test_debug_validation(lib):

@@ -14,7 +14,8 @@ import torch
 import oracle
 import structured_sparse_long_gb300 as pa
 from structured_sparse_long_gb300 import build as pbuild
-from structured_sparse_long_gb300.synth import MODE_ECP, MODE_PI, WORKLOADS, make_inputs, small_case
+from structured_sparse_long_gb300.synth import (MODE_ECP, MODE_PI, MODE_PI_BIDIR, WORKLOADS, make_inputs,
+                                                small_case)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,7 +77,7 @@ def check_forward(w, inputs=None):
 
 # ----------------------------------------------------------------------------- the five workloads
 
-@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C6"])
 def test_workload_forward_matches_oracle(name):
     check_forward(WORKLOADS[name])
 
@@ -120,6 +121,20 @@ SMALL = [
     ("d32-bf16", 1, 2, 2, 150, 32, 10, 20, 3, MODE_PI, "bf16"),
     ("f32-d64", 1, 2, 1, 200, 64, 30, 40, 2, MODE_PI, "f32"),
     ("f32-d128-ecp", 1, 2, 2, 130, 128, 20, 0, 0, MODE_ECP, "f32"),
+    # bidirectional band i-k..i+k and skips i -/+ m*pi
+    ("bi-ragged-d64", 1, 2, 2, 300, 64, 40, 64, 2, MODE_PI_BIDIR, "bf16"),
+    ("bi-gqa4-d128", 1, 8, 2, 257, 128, 64, 96, 4, MODE_PI_BIDIR, "bf16"),
+    ("bi-gqa2-d64", 1, 4, 2, 190, 64, 31, 50, 2, MODE_PI_BIDIR, "bf16"),
+    ("bi-k0", 1, 2, 2, 100, 64, 0, 7, 5, MODE_PI_BIDIR, "bf16"),
+    ("bi-S0", 1, 2, 2, 200, 64, 70, 1, 0, MODE_PI_BIDIR, "bf16"),
+    ("bi-overlap", 1, 2, 2, 200, 64, 40, 16, 5, MODE_PI_BIDIR, "bf16"),
+    ("bi-N<k", 1, 2, 2, 50, 64, 128, 256, 1, MODE_PI_BIDIR, "bf16"),
+    ("bi-N<pi", 1, 2, 2, 90, 128, 16, 100, 2, MODE_PI_BIDIR, "bf16"),
+    ("bi-wide-band", 1, 2, 2, 260, 64, 1000, 8, 2, MODE_PI_BIDIR, "bf16"),
+    ("bi-tiny-N", 1, 1, 1, 1, 64, 8, 4, 2, MODE_PI_BIDIR, "bf16"),
+    ("bi-long-d128", 1, 4, 1, 1500, 128, 100, 256, 3, MODE_PI_BIDIR, "bf16"),
+    ("bi-d32-bf16", 1, 2, 2, 150, 32, 10, 20, 3, MODE_PI_BIDIR, "bf16"),
+    ("bi-f32-d64", 1, 2, 1, 200, 64, 30, 40, 2, MODE_PI_BIDIR, "f32"),
 ]
 
 
@@ -150,7 +165,7 @@ def test_counts_bit_exact(spec):
     np.testing.assert_array_equal(isum.cpu().numpy(), exp_i)
 
 
-@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5"])
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5", "C6"])
 def test_workload_counts_bit_exact(name):
     w = WORKLOADS[name]
     inp = make_inputs(w, with_dout=False)
@@ -168,7 +183,7 @@ def test_workload_counts_bit_exact(name):
 
 PROB_CASES = [s for s in SMALL if s[4] <= 400 and s[0] in
               ("ragged-d64", "gqa4-d128", "overlap", "ecp-ragged", "d32-bf16", "f32-d64", "N<k",
-               "gqa3-d64")]
+               "gqa3-d64", "bi-gqa4-d128", "bi-overlap", "bi-f32-d64")]
 
 
 @pytest.mark.parametrize("spec", PROB_CASES, ids=[s[0] for s in PROB_CASES])
@@ -205,6 +220,21 @@ def test_alpha_edges():
     a[:, 1, ::4] = 1.0
     inp["alpha"] = a
     check_forward(ff, inp)
+
+
+def test_bidirectional_backward_is_refused():
+    """The backward covers the causal and ECP modes; the bidirectional mode returns
+    PI_ERR_UNSUPPORTED before anything is launched."""
+    w = small(("bi-bwd", 1, 2, 2, 64, 64, 8, 16, 1, MODE_PI_BIDIR, "bf16"))
+    inp = make_inputs(w, with_dout=True)
+    dev = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    out, lse = pa.fwd(dev["q"], dev["k"], dev["v"], dev["alpha"], w.k_local, w.period, w.S, w.mode)
+    with pytest.raises(pa.PiAttnError) as e:
+        pa.bwd(dev["q"], dev["k"], dev["v"], dev["alpha"], out, lse, dev["dout"], w.k_local,
+               w.period, w.S, w.mode)
+    assert e.value.code == -3
+    torch.cuda.synchronize()
+    assert pa.status() == 0
 
 
 def test_forward_is_deterministic():

