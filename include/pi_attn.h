@@ -185,6 +185,23 @@ int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float
                         int mode, void *dq, void *dk, void *dv, float *dalpha, void *stream);
 
 /*
+ * pi_attn_decode -- one decode step against a KV cache: for every batch entry b
+ * and query head h, row i = N - 1 of pi_attn_fwd, where the cache already holds
+ * the key and value rows 0 .. N-1 (the new token's own row at N - 1).  Causal pi
+ * mode or ECP mode (bidirectional: PI_ERR_UNSUPPORTED; the future does not exist
+ * yet).  The neighbour set of row N-1 is the band rows max(0, N-1-k_local) .. N-1
+ * (ECP: the half-segments of row N-1) and the skip rows N-1 - m*period with
+ * m*period > k_local, so only those rows of the cache are read.
+ *   q [B,H,d] bf16 (the new queries), k_cache and v_cache [B,Hkv,N,d] bf16 (the
+ *   layout of pi_attn_fwd's k and v), alpha [B,H] fp32 (the new token's gate;
+ *   NULL in ECP mode), out [B,H,d] bf16, lse [B,H] fp32.  d in {64, 128};
+ *   H / Hkv <= 16.  Same ownership, asynchrony and error rules as pi_attn_fwd.
+ */
+int pi_attn_decode(const void *q, const void *k_cache, const void *v_cache, const float *alpha,
+                   int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
+                   void *out, float *lse, void *stream);
+
+/*
  * pi_attn_status -- synchronises `stream`, reads the current device's status
  * word, resets it to PI_OK and returns what it held (PI_OK or
  * PI_ERR_DEVICE_TIMEOUT), or PI_ERR_CUDA if the synchronisation failed.

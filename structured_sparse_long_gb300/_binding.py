@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
         lib.pi_attn_debug_wait_timeout.argtypes = [I, P]
         lib.pi_attn_debug_trace.argtypes = [P, P, P, P] + [I] * 9 + [P, P, P, I, P]
         lib.pi_attn_debug_trace.restype = I
+        lib.pi_attn_decode.argtypes = [P, P, P, P] + [I] * 9 + [P, P, P]
+        lib.pi_attn_decode.restype = I
         for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
                      "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
                      "pi_attn_debug_wait_timeout"):
@@ -135,6 +137,31 @@ def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
     rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d, k_local, period, S, mode,
             _ptr(out), _ptr(lse), _stream(stream))
     _check(fn.__name__, rc)
+    return out, lse
+
+
+def decode(q, k_cache, v_cache, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
+           out=None, lse=None, stream=None):
+    """pi_attn_decode: q [B,H,d] bf16 against the cache k_cache/v_cache [B,Hkv,N,d] bf16
+    (row N-1 of the forward). Returns (out [B,H,d], lse [B,H])."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B,H,d] and the caches [B,Hkv,N,d]")
+    B, H, d = q.shape
+    Hkv, N = k_cache.shape[1], k_cache.shape[2]
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _expect(t, n, torch.bfloat16)
+    _expect(v_cache, "v_cache", torch.bfloat16, k_cache.shape)
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    _expect(out, "out", torch.bfloat16, q.shape)
+    _expect(lse, "lse", torch.float32, (B, H))
+    rc = load().pi_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(alpha), B, H, Hkv, N, d,
+                               k_local, period, S, mode, _ptr(out), _ptr(lse), _stream(stream))
+    _check("pi_attn_decode", rc)
     return out, lse
 
 

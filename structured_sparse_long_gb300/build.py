@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpi_attn.so")
 
-SOURCES = ["api.cu", "pi_simt.cu", "pi_fwd_tc.cu", "pi_bwd_tc.cu"]
+SOURCES = ["api.cu", "pi_simt.cu", "pi_fwd_tc.cu", "pi_bwd_tc.cu", "pi_decode.cu"]
 HEADERS = ["pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -199,6 +199,28 @@ int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float
                    false);
 }
 
+int pi_attn_decode(const void *q, const void *k_cache, const void *v_cache, const float *alpha, int B,
+                   int H, int Hkv, int N, int d, int k_local, int period, int S, int mode, void *out,
+                   float *lse, void *stream) {
+    if (!q || !k_cache || !v_cache || !out || !lse) return PI_ERR_NULL;
+    if (mode != PI_MODE_ECP && !alpha) return PI_ERR_NULL;
+    const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    if (rc != PI_OK) return rc;
+    if (mode == PI_MODE_PI_BIDIR || (d != 64 && d != 128) || H / Hkv > 16) return PI_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * N * d > (1LL << 62)) return PI_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return PI_ERR_ALIGN;
+    if (!aligned(lse, 4) || (alpha && !aligned(alpha, 4))) return PI_ERR_ALIGN;
+    int *status = status_word();
+    if (!status) return PI_ERR_CUDA;
+    pi::LaunchDecode L;
+    L.q = q; L.k = k_cache; L.v = v_cache; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
+    L.out = out; L.lse = lse;
+    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    L.status = status; L.timeout_ns = kWaitTimeoutNs;
+    return map_cuda(pi::launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
 int pi_attn_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PI_ERR_CUDA;
     int *status = status_word();

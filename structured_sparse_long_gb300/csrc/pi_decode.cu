@@ -1,0 +1,365 @@
+// pi_decode.cu -- one decode step of pi-Attention / ECP attention against a KV cache.
+//
+// What it computes: row i = N-1 of the forward ("pi-Attention: Periodic Sparse Transformers for
+// Efficient Long-Context Modeling", section 2.1-2.3, causal form; ECP page, section 2), for a
+// new query per (batch entry, head) whose key/value rows 0 .. N-1 -- its own included -- are in
+// the cache: one softmax over the band rows lo .. N-1 and the skip rows N-1 - m*period, with
+// log2(alpha) on band logits and log2(1 - alpha) on skip logits.
+//
+// How (HBM-bound gather, no dense contraction):
+//   * The key list of row N-1 is the band (one contiguous run of cache rows) followed by the
+//     skip rows; it is cut into 32-key chunks.  A cluster of P CTAs serves one (batch entry,
+//     KV head); CTA r takes chunks r, r+P, ...  so that small batches still fill the GPU.
+//   * Thread 0 stages each chunk's K and V rows in shared memory with bulk copies
+//     (cp.async.bulk, one per contiguous band run and one per skip row) into a two-stage ring
+//     completed by an mbarrier.
+//   * Warp w handles the query heads w, w+4, ... of the GQA group.  Lanes split d for the dot
+//     products (conflict-free 256-byte row reads), a butterfly reduce-scatter leaves lane t
+//     with the score of key t, and the warp keeps an online softmax state per head.
+//   * The P partial states (m, l, o) of a head are merged by CTA 0 of the cluster through
+//     distributed shared memory, which writes out (bf16) and lse.
+//   * Every mbarrier wait is bounded; a CTA that gives up still takes part in both cluster
+//     barriers, so its cluster never waits forever.
+#include <cuda.h>
+
+#include "pi_common.cuh"
+#include "pi_launch.h"
+#include "pi_tc_ptx.cuh"
+
+namespace pi {
+namespace dec {
+
+using tc::mbar_init;
+using tc::mbar_expect_tx;
+using tc::wait_bar;
+using tc::WaitCtx;
+
+constexpr int WARPS = 4;
+constexpr int THREADS = WARPS * 32;
+constexpr int KEYS = 32;     // keys per chunk: one lane per key
+constexpr int MAX_P = 8;     // CTAs per cluster (portable limit)
+constexpr int MAX_G = 16;    // query heads per KV head
+constexpr unsigned kFull = 0xffffffffu;
+
+struct DecArgs {
+    const __nv_bfloat16 *q, *k, *v;  // q [B,H,d]; k, v [B,Hkv,N,d]
+    const float *alpha;              // [B,H] or null (ECP)
+    __nv_bfloat16 *out;              // [B,H,d]
+    float *lse;                      // [B,H]
+    Shape s;                         // N is the cache length; the query sits at position N-1
+    int lo, n_band, n_keys, m_first, n_chunks;
+    int *status;
+    uint64_t timeout_ns;
+};
+
+template <int D>
+struct Lay {
+    static constexpr int ROW = D * 2;                       // bytes of one bf16 row
+    static constexpr int STAGE = 2 * KEYS * ROW;            // K then V rows of one chunk
+    static constexpr int PART_OFF = 2 * STAGE;              // partial states after the ring
+    static constexpr int PART = (D + 2) * 4;                // m, l, o[D] of one head (fp32)
+    static constexpr int BAR_OFF = PART_OFF + MAX_G * PART; // full[2], abort flag
+    static constexpr int BYTES = BAR_OFF + 32;
+};
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// E consecutive bf16 of a shared-memory row (E = 2 or 4: one 4- or 8-byte load) as fp32.
+template <int E>
+__device__ __forceinline__ void lds_bf16(const uint8_t *p, float *f) {
+    if (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        f[0] = __uint_as_float(u << 16);
+        f[1] = __uint_as_float(u & 0xffff0000u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
+    using L = Lay<D>;
+    constexpr int E = D / 32;  // columns per lane
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::BAR_OFF + 16);
+    float *part = reinterpret_cast<float *>(smem + L::PART_OFF);
+
+    const Shape &s = a.s;
+    const int P = gridDim.x;
+    const int r = (int)cluster_rank();
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int G = s.H / s.Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const WaitCtx wc{abort_flag, a.status, a.timeout_ns};
+    const size_t plane = ((size_t)b * s.Hkv + g) * (size_t)s.N * D;
+    const __nv_bfloat16 *kp = a.k + plane, *vp = a.v + plane;
+    const int n_local = (a.n_chunks > r) ? (a.n_chunks - r + P - 1) / P : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        *abort_flag = 0u;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+
+    // key list position t -> cache row
+    auto key_row = [&](int t) -> int {
+        return t < a.n_band ? a.lo + t : (s.N - 1) - (a.m_first + t - a.n_band) * s.period;
+    };
+    // chunk c of this CTA (global chunk r + c*P) into ring stage c & 1 (thread 0 only)
+    int issued = 0;
+    auto issue = [&](int c) {
+        issued = c + 1;
+        const int qc = r + c * P, st = c & 1;
+        const int t0 = qc * KEYS, t1 = min(t0 + KEYS, a.n_keys);
+        const uint32_t sk = sbase + st * L::STAGE, sv = sk + KEYS * L::ROW;
+        const uint32_t bar = bar0 + 8 * st;
+        mbar_expect_tx(bar, (uint32_t)(t1 - t0) * 2u * L::ROW);
+        const int tb = min(t1, a.n_band);
+        if (t0 < tb) {  // band rows: one contiguous run
+            const size_t row0 = (size_t)(a.lo + t0) * D;
+            const uint32_t bytes = (uint32_t)(tb - t0) * L::ROW;
+            bulk_g2s(sk, kp + row0, bytes, bar);
+            bulk_g2s(sv, vp + row0, bytes, bar);
+        }
+        for (int t = max(t0, a.n_band); t < t1; ++t) {  // skip rows, one by one
+            const size_t row = (size_t)key_row(t) * D;
+            bulk_g2s(sk + (t - t0) * L::ROW, kp + row, L::ROW, bar);
+            bulk_g2s(sv + (t - t0) * L::ROW, vp + row, L::ROW, bar);
+        }
+    };
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < min(2, n_local); ++c) issue(c);
+    }
+
+    // ---- per-warp heads: query slice, prior, online state
+    constexpr int HPW = MAX_G / WARPS;  // at most 4 heads per warp
+    float qv[HPW][E], o[HPW][E], m[HPW], l[HPW], offb[HPW], offs[HPW];
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+        const int hh = warp + WARPS * j;
+        m[j] = -INFINITY;
+        l[j] = 0.f;
+        offb[j] = 0.f;
+        offs[j] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < E; ++e) { qv[j][e] = 0.f; o[j][e] = 0.f; }
+        if (hh < G) {
+            const int h = g * G + hh;
+            const __nv_bfloat16 *qr = a.q + ((size_t)b * s.H + h) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) qv[j][e] = __bfloat162float(qr[e]) * s.scale_log2;
+            if (a.alpha) {
+                const float al = a.alpha[(size_t)b * s.H + h];
+                offb[j] = log2f(al);
+                offs[j] = log2f(1.f - al);
+            }
+        }
+    }
+
+    bool ok = true;
+    for (int c = 0; c < n_local; ++c) {
+        const int st = c & 1;
+        ok = wait_bar(bar0 + 8 * st, (c >> 1) & 1, wc);
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        const int t0 = (r + c * P) * KEYS;
+        const int nk = min(KEYS, a.n_keys - t0);
+        const bool band_key = t0 + lane < a.n_band;
+        const uint8_t *sk = smem + st * L::STAGE, *sv = sk + KEYS * L::ROW;
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+            if (warp + WARPS * j >= G) break;  // uniform per warp
+            // partial dot products of the 32 keys over this lane's columns
+            float pd[KEYS];
+#pragma unroll
+            for (int t = 0; t < KEYS; ++t) {
+                float acc = 0.f;
+                if (t < nk) {
+                    float kf[E];
+                    lds_bf16<E>(sk + t * L::ROW + lane * E * 2, kf);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc = fmaf(qv[j][e], kf[e], acc);
+                }
+                pd[t] = acc;
+            }
+            // butterfly reduce-scatter: lane t ends with the full score of key t
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const float send = up ? pd[i] : pd[i + w];
+                    const float keep = up ? pd[i + w] : pd[i];
+                    pd[i] = keep + __shfl_xor_sync(kFull, send, w);
+                }
+            }
+            const float z = (lane < nk) ? pd[0] + (band_key ? offb[j] : offs[j]) : -INFINITY;
+            float mx = z;
+#pragma unroll
+            for (int w = 16; w; w >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, w));
+            const float mn = fmaxf(m[j], mx);
+            if (mn == -INFINITY) continue;  // nothing finite yet (uniform)
+            const float corr = exp2f(m[j] - mn);
+            const float p = exp2f(z - mn);
+            float ps = p;
+#pragma unroll
+            for (int w = 16; w; w >>= 1) ps += __shfl_xor_sync(kFull, ps, w);
+            l[j] = l[j] * corr + ps;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[j][e] *= corr;
+            for (int t = 0; t < nk; ++t) {
+                const float pt = __shfl_sync(kFull, p, t);
+                float vf[E];
+                lds_bf16<E>(sv + t * L::ROW + lane * E * 2, vf);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[j][e] = fmaf(pt, vf[e], o[j][e]);
+            }
+            m[j] = mn;
+        }
+        __syncthreads();  // stage st is free again
+        if (threadIdx.x == 0 && c + 2 < n_local) issue(c + 2);
+    }
+    if (!ok && threadIdx.x == 0) {  // let copies in flight (the last two issued) land first
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, nullptr, 20000000ull};
+        for (int c = max(0, issued - 2); c < issued; ++c) wait_bar(bar0 + 8 * (c & 1), (c >> 1) & 1, w2);
+    }
+
+    // ---- partial states to shared memory, merged by CTA 0 of the cluster
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+        const int hh = warp + WARPS * j;
+        if (hh >= G) break;
+        float *ps = part + hh * (D + 2);
+        if (lane == 0) {
+            ps[0] = ok ? m[j] : -INFINITY;
+            ps[1] = ok ? l[j] : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) ps[2 + lane * E + e] = ok ? o[j][e] : 0.f;
+    }
+    cluster_sync();
+    if (r == 0) {
+        for (int hh = warp; hh < G; hh += WARPS) {
+            const uint32_t pa = sbase + L::PART_OFF + hh * (D + 2) * 4;
+            float mr[MAX_P];
+            float mt = -INFINITY;
+            for (int x = 0; x < P; ++x) {
+                mr[x] = ld_dsmem(pa, x);
+                mt = fmaxf(mt, mr[x]);
+            }
+            float lt = 0.f, ot[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) ot[e] = 0.f;
+            if (mt != -INFINITY) {
+                for (int x = 0; x < P; ++x) {
+                    if (mr[x] == -INFINITY) continue;
+                    const float f = exp2f(mr[x] - mt);
+                    lt += f * ld_dsmem(pa + 4, x);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) ot[e] += f * ld_dsmem(pa + (2 + lane * E + e) * 4, x);
+                }
+            }
+            const int h = g * G + hh;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            __nv_bfloat16 *orow = a.out + ((size_t)b * s.H + h) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) orow[e] = __float2bfloat16_rn(ot[e] * inv);
+            if (lane == 0) a.lse[(size_t)b * s.H + h] = lt > 0.f ? (mt + log2f(lt)) * kLn2 : -INFINITY;
+        }
+    }
+    cluster_sync();  // the other CTAs' shared memory stays alive until CTA 0 has read it
+}
+
+template <int D>
+static cudaError_t launch(const DecArgs &a, int P, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P, (unsigned)a.s.Hkv, (unsigned)a.s.B);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Lay<D>::BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D>, a);
+}
+
+}  // namespace dec
+
+cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st) {
+    using namespace dec;
+    const Shape &s = L.s;
+    const int G = s.H / s.Hkv;
+    if (G > MAX_G || s.Hkv > 65535 || s.B > 65535) return cudaErrorInvalidConfiguration;
+    DecArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(L.q);
+    a.k = static_cast<const __nv_bfloat16 *>(L.k);
+    a.v = static_cast<const __nv_bfloat16 *>(L.v);
+    a.alpha = L.alpha;
+    a.out = static_cast<__nv_bfloat16 *>(L.out);
+    a.lse = L.lse;
+    a.s = s;
+    a.status = L.status;
+    a.timeout_ns = L.timeout_ns;
+    // the key list of row N-1: band lo .. N-1, then skips N-1 - m*period with m*period > k
+    const int i = s.N - 1;
+    a.lo = band_lo(i, s.mode, s.k_local);
+    a.n_band = i - a.lo + 1;
+    a.m_first = 1;
+    int n_skip = 0;
+    if (s.mode != kModeEcp && s.S > 0) {
+        a.m_first = s.k_local / s.period + 1;
+        const int m_last = min(s.S, i / s.period);
+        n_skip = max(0, m_last - a.m_first + 1);
+    }
+    a.n_keys = a.n_band + n_skip;
+    a.n_chunks = (a.n_keys + KEYS - 1) / KEYS;
+    // cluster size: enough CTAs for about two per SM, at most one chunk each, at most 8
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 1;
+    }
+    const long long pairs = (long long)s.B * s.Hkv;
+    int P = (int)std::min<long long>(MAX_P, std::max<long long>(1, (2LL * sms + pairs - 1) / pairs));
+    P = std::max(1, std::min(P, a.n_chunks));
+    if (s.d == 64) return launch<64>(a, P, st);
+    if (s.d == 128) return launch<128>(a, P, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pi

@@ -39,6 +39,16 @@ struct LaunchBwd {
     bool fp32;
 };
 
+struct LaunchDecode {
+    const void *q, *k, *v;  // q [B,H,d]; k, v the cache [B,Hkv,N,d]
+    const float *alpha;     // [B,H] or null (ECP)
+    void *out;              // [B,H,d]
+    float *lse;             // [B,H]
+    Shape s;
+    int *status;
+    uint64_t timeout_ns;
+};
+
 // CUDA-core kernels (pi_simt.cu)
 cudaError_t launch_fwd_simt(const LaunchFwd &L, cudaStream_t st);
 cudaError_t launch_bwd_simt(const LaunchBwd &L, cudaStream_t st);
@@ -54,6 +64,9 @@ cudaError_t launch_bwd_dkdv_tc(const LaunchBwd &L, int *status, uint64_t timeout
 // tcgen05 / TMEM / TMA forward, bf16, d in {64, 128} (pi_fwd_tc.cu).
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st);
+
+// decode step against a KV cache, bf16, d in {64, 128} (pi_decode.cu)
+cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st);
 
 // bounded-wait self test (pi_fwd_tc.cu)
 cudaError_t launch_wait_timeout_probe(int *status, uint64_t timeout_ns, cudaStream_t st);

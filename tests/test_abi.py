@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
               "pi_attn_bwd_workspace_size", "pi_attn_status", "pi_attn_strerror",
-              "pi_attn_debug_counts", "pi_attn_debug_probs", "pi_attn_debug_wait_timeout"):
+              "pi_attn_debug_counts", "pi_attn_debug_probs", "pi_attn_debug_wait_timeout",
+              "pi_attn_decode", "pi_attn_bwd_noalloc", "pi_attn_debug_trace"):
         assert n in names
 
 
@@ -106,6 +107,27 @@ def test_bwd_validation(lib, fn):
     assert bwd_call(lib, ws=None, fn=fn) == PI_ERR_WORKSPACE
     assert bwd_call(lib, ws_bytes=16, fn=fn) == PI_ERR_WORKSPACE
     assert bwd_call(lib, mode=2, fn=fn) == PI_ERR_UNSUPPORTED  # the backward is causal/ECP only
+
+
+def dec_call(lib, q=A16, kc=A16, vc=A16, alpha=A16, B=1, H=4, Hkv=2, N=64, d=64, kl=8, per=16, S=1,
+             mode=0, out=A16, lse=A16):
+    return lib.pi_attn_decode(q, kc, vc, alpha, B, H, Hkv, N, d, kl, per, S, mode, out, lse, None)
+
+
+def test_decode_validation(lib):
+    assert dec_call(lib, q=None) == PI_ERR_NULL
+    assert dec_call(lib, kc=None) == PI_ERR_NULL
+    assert dec_call(lib, lse=None) == PI_ERR_NULL
+    assert dec_call(lib, alpha=None) == PI_ERR_NULL               # pi mode needs alpha
+    assert dec_call(lib, N=0) == PI_ERR_SHAPE
+    assert dec_call(lib, H=3, Hkv=2) == PI_ERR_SHAPE
+    assert dec_call(lib, mode=1, kl=0, S=0, alpha=None) == PI_ERR_SHAPE
+    assert dec_call(lib, mode=2) == PI_ERR_UNSUPPORTED              # bidirectional has no decode
+    assert dec_call(lib, d=32) == PI_ERR_UNSUPPORTED
+    assert dec_call(lib, H=34, Hkv=2) == PI_ERR_UNSUPPORTED         # 17 query heads per KV head
+    assert dec_call(lib, q=A16 + 8) == PI_ERR_ALIGN
+    assert dec_call(lib, vc=A16 + 4) == PI_ERR_ALIGN
+    assert dec_call(lib, lse=A16 + 2) == PI_ERR_ALIGN
 
 
 def test_debug_validation(lib):
