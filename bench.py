@@ -65,8 +65,24 @@ def pairs_per_head(N, k, period, S, mode) -> int:
     return band + skip
 
 
+def decode_keys(w) -> int:
+    """Neighbours of row N-1 (the decode query): band rows and skip rows N-1 - m*period."""
+    i = w.N - 1
+    if w.mode == MODE_ECP:
+        return i - max(0, (i // w.k_local - 1) * w.k_local) + 1
+    band = min(w.k_local, i) + 1
+    skip = sum(1 for m in range(1, w.S + 1) if m * w.period > w.k_local and i - m * w.period >= 0)
+    return band + skip
+
+
 def work(w, backward: bool):
     esz = 4 if w.dtype == "f32" else 2
+    if w.decode:  # only the neighbour rows of the cache are read
+        nk = decode_keys(w)
+        pairs = w.B * w.H * nk
+        byts = w.B * w.Hkv * nk * w.d * esz * 2 + 2 * w.B * w.H * w.d * esz + 8 * w.B * w.H
+        return {"pairs": pairs, "fwd_bytes": byts, "fwd_flops": 4 * w.d * pairs, "bytes": byts,
+                "flops": 4 * w.d * pairs}
     pairs = pairs_per_head(w.N, w.k_local, w.period, w.S, w.mode) * w.B * w.H
     qo = w.B * w.H * w.N * w.d * esz
     kv = w.B * w.Hkv * w.N * w.d * esz
@@ -94,7 +110,9 @@ def load_peaks():
 KERNEL_SOURCES = {
     "fwd": ("pi_fwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"),
     "bwd": ("pi_bwd_tc.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"),
+    "dec": ("pi_decode.cu", "pi_common.cuh", "pi_launch.h", "pi_tc_ptx.cuh"),
 }
+PROFILE_NAMES = {"fwd": "pi_fwd_tc", "bwd": "pi_bwd_tc", "dec": "pi_decode"}
 
 
 def kernel_source_sha(kind: str = "fwd") -> str:
@@ -106,10 +124,10 @@ def kernel_source_sha(kind: str = "fwd") -> str:
 
 
 def profiled_traffic(workload: str, kind: str = "fwd"):
-    """DRAM bytes of one forward launch (kind "fwd") or of one backward call, both of its
-    kernels (kind "bwd"), from a committed ncu summary -- if it was taken on the current
-    kernel source (else None)."""
-    path = os.path.join(PROFILE_DIR, f"pi_{kind}_tc_{workload}.md")
+    """DRAM bytes of one forward launch (kind "fwd"), of one backward call, both of its
+    kernels (kind "bwd"), or of one decode step (kind "dec"), from a committed ncu summary --
+    if it was taken on the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"{PROFILE_NAMES[kind]}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -219,12 +237,59 @@ class OracleSample:
         return text
 
 
+class DecodeOracleSample:
+    """The fp64 oracle on this host's cores for the decode step of `nb` sequences: row N-1 of
+    the forward.  Only the last max(k, S*period) + 1 cache rows can be neighbours of row N-1,
+    so the oracle gets that window (the query at its last row), which leaves every key
+    distance unchanged."""
+
+    def __init__(self, w):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.inp = make_inputs(w, with_dout=False)
+        self.cores = oracle.threads()
+        self.W = min(w.N, max(w.k_local, w.S * w.period) + 1)
+
+    def run(self, nb: int) -> float:
+        w, W = self.w, self.W
+        q = torch.zeros(nb, w.H, W, w.d, dtype=self.inp["q"].dtype)
+        q[:, :, W - 1] = self.inp["q"][:nb]
+        a = None
+        if self.inp["alpha"] is not None:
+            a = torch.full((nb, w.H, W), 0.5, dtype=torch.float32)
+            a[:, :, W - 1] = self.inp["alpha"][:nb]
+        k = self.inp["k"][:nb, :, w.N - W:].contiguous()
+        v = self.inp["v"][:nb, :, w.N - W:].contiguous()
+        t0 = time.perf_counter()
+        self.oracle.fwd(q, k, v, a, w.k_local, w.period, w.S, w.mode, rows=(W - 1, W))
+        return time.perf_counter() - t0
+
+    def size_for(self, target_s: float) -> int:
+        t_cal = self.run(1)
+        return int(min(self.w.B, max(1, target_s / max(t_cal, 1e-6))))
+
+    def describe(self, nb: int) -> str:
+        return (f"fp64 oracle decode step (row N-1 over the last {self.W} cache rows) of {nb} of "
+                f"{self.w.B} sequences, all {self.w.H} heads; tokens/s = {nb}/t")
+
+
+def oracle_sample(w):
+    return DecodeOracleSample(w) if w.decode else OracleSample(w)
+
+
+def tokens_per_unit(w) -> int:
+    """Tokens one sample unit stands for: a position of every batch entry, or one sequence."""
+    return 1 if w.decode else w.B
+
+
 def cpu_baseline(w, target_s=10.0):
     """Returns (tokens/s, cores, sample description) of the oracle on a bounded sample."""
-    smp = OracleSample(w)
-    npos = smp.size_for(target_s)
-    t = smp.run(npos)
-    return w.B * npos / t, smp.cores, smp.describe(npos)
+    smp = oracle_sample(w)
+    n = smp.size_for(target_s)
+    t = smp.run(n)
+    return tokens_per_unit(w) * n / t, smp.cores, smp.describe(n)
 
 
 def reduce_max(x: float, world: int, device="cpu") -> float:
@@ -240,12 +305,12 @@ def reference_arm(args, w, rank, world):
     """The oracle as the reference implementation: rank 0 only, on host cores."""
     if rank != 0:
         return
-    smp = OracleSample(w)
+    smp = oracle_sample(w)
     npos = smp.size_for(min(8.0, 150.0 / (args.warmup + args.steps)))
     for _ in range(args.warmup):
         smp.run(npos)
     per_step = [smp.run(npos) for _ in range(args.steps)]
-    value = w.B * npos * len(per_step) / sum(per_step)
+    value = tokens_per_unit(w) * npos * len(per_step) / sum(per_step)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(per_step) / len(per_step), "higher_is_better": True,
@@ -282,7 +347,7 @@ def gpu_arm(args, w, rank, world, local_rank):
     inp = make_inputs(w, with_dout=w.backward)
     d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
     out = torch.empty_like(d["q"])
-    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    lse = torch.empty((w.B, w.H) if w.decode else (w.B, w.H, w.N), device=dev, dtype=torch.float32)
     bufs = {}
     if w.backward:
         bufs = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]),
@@ -300,8 +365,15 @@ def gpu_arm(args, w, rank, world, local_rank):
                w.mode, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], dalpha=bufs["dalpha"],
                workspace=bufs["ws"], stream=stream)
 
+    def dec():
+        pa.decode(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
+                  lse=lse, stream=stream)
+
     # (name, launcher, kernels it launches)
-    phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 3)] if w.backward else [])
+    if w.decode:
+        phases = [("pi_attn_decode", dec, 1)]
+    else:
+        phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 3)] if w.backward else [])
     wk = work(w, w.backward)
     flush = wk["bytes"] < 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, device=dev, dtype=torch.float32) if flush else None
@@ -349,7 +421,7 @@ def gpu_arm(args, w, rank, world, local_rank):
     total_ms = sum(step_ms)
     total_ms = reduce_max(total_ms, world, dev if args.backend == "nccl" else "cpu")
     ms_per_step = total_ms / args.steps
-    tokens_per_step = w.B * w.N * world
+    tokens_per_step = (w.B if w.decode else w.B * w.N) * world
     value = tokens_per_step * args.steps / (total_ms / 1e3)
     tflops = wk["flops"] * world * args.steps / (total_ms / 1e3) / 1e12
 
@@ -357,8 +429,8 @@ def gpu_arm(args, w, rank, world, local_rank):
     peaks, peak_kind = load_peaks()
     dom = max(per_phase, key=lambda n: sum(per_phase[n]))
     dom_ms = statistics.mean(per_phase[dom])
-    dom_bytes = wk["fwd_bytes"] if dom == "pi_attn_fwd" else wk["bwd_bytes"]
-    dom_flops = wk["fwd_flops"] if dom == "pi_attn_fwd" else wk["bwd_flops"]
+    dom_bytes = wk["bwd_bytes"] if dom == "pi_attn_bwd" else wk["fwd_bytes"]
+    dom_flops = wk["bwd_flops"] if dom == "pi_attn_bwd" else wk["fwd_flops"]
     hbm = peaks["hbm_gbs"]
     tensor = peaks["bf16_tflops"]
     t_hbm = dom_bytes / (hbm * 1e9)
@@ -368,7 +440,8 @@ def gpu_arm(args, w, rank, world, local_rank):
         achieved, peak, unit = dom_bytes / (dom_ms / 1e3) / 1e9, hbm, "GB/s"
     else:
         achieved, peak, unit = dom_flops / (dom_ms / 1e3) / 1e12, tensor, "TFLOP/s"
-    traffic = profiled_traffic(w.name, "fwd" if dom == "pi_attn_fwd" else "bwd")
+    traffic = profiled_traffic(w.name, {"pi_attn_fwd": "fwd", "pi_attn_bwd": "bwd",
+                                        "pi_attn_decode": "dec"}[dom])
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                 "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}, burst)",
@@ -380,7 +453,13 @@ def gpu_arm(args, w, rank, world, local_rank):
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host = {n: (t.pin_memory() if t is not None else None) for n, t in inp.items()}
+        if w.decode:  # per step: the new queries and gates, and the new token's K/V rows
+            host = {"q": inp["q"], "alpha": inp["alpha"],
+                    "k_new": inp["k"][:, :, w.N - 1].contiguous(),
+                    "v_new": inp["v"][:, :, w.N - 1].contiguous()}
+            host = {n: (t.pin_memory() if t is not None else None) for n, t in host.items()}
+        else:
+            host = {n: (t.pin_memory() if t is not None else None) for n, t in inp.items()}
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for n, t in host.items()
@@ -394,7 +473,11 @@ def gpu_arm(args, w, rank, world, local_rank):
 
         def e2e_step():
             for n, t in host.items():
-                if t is not None and (n != "dout" or w.backward):
+                if t is None or (n == "dout" and not w.backward):
+                    continue
+                if n in ("k_new", "v_new"):  # append the new token to the cache (row N-1)
+                    d[n[0]][:, :, w.N - 1].copy_(t, non_blocking=True)
+                else:
                     d[n].copy_(t, non_blocking=True)
             step()
             out_h.copy_(out, non_blocking=True)

@@ -14,6 +14,8 @@ Context Propagating Perceiver Architectures...", section 2, PAR block):
   C5  training fwd+bwd bf16       B2 H16 Hkv16 N16384 d64  k256 pi512  S2
   C6  bidirectional GQA bf16 fwd  B1 H16 Hkv4  N65536 d128 k256 pi1024 S4 (band i-k..i+k,
                                   skips i -/+ m*pi: the general form of the same page, 2.1-2.2)
+  D4  decode step, C4 layer       B64 H16 Hkv4 cache N16384 d128 k256 pi1024 S4: one new
+                                  query per sequence (q [B,H,d], alpha [B,H]) against the cache
 
 Draw order per workload: q, k, v, alpha, dout, from one CPU torch.Generator
 seeded with the workload's seed.  Values are drawn in fp32 and then cast to
@@ -50,6 +52,7 @@ class Workload:
     alpha: str            # "uniform(a,b)", "sigmoid(sigma)" or "none"
     backward: bool = False
     description: str = ""
+    decode: bool = False  # one new query per (b, h) against a KV cache of N rows (row N-1)
 
     @property
     def tokens(self) -> int:
@@ -77,6 +80,9 @@ WORKLOADS = {
     "C6": Workload("C6", 1, 16, 4, 65536, 128, 256, 1024, 4, MODE_PI_BIDIR, "bf16", 5, "unit",
                    "sigmoid(1.5)",
                    description="long-context GQA bf16 bidirectional pi-Attention fwd"),
+    "D4": Workload("D4", 64, 16, 4, 16384, 128, 256, 1024, 4, MODE_PI, "bf16", 6, "unit",
+                   "sigmoid(1.5)", decode=True,
+                   description="decode step of the long-context GQA layer, 64 sequences"),
 }
 
 
@@ -104,6 +110,7 @@ def make_inputs(w: Workload, with_dout: Optional[bool] = None, device="cpu") -> 
 
     Returns a dict of contiguous tensors: q [B,H,N,d], k and v [B,Hkv,N,d]
     (dtype of the workload), alpha [B,H,N] fp32 or None, dout [B,H,N,d] or None.
+    A decode workload has q [B,H,d] and alpha [B,H] instead (k and v are the cache).
     """
     if with_dout is None:
         with_dout = w.backward
@@ -118,11 +125,18 @@ def make_inputs(w: Workload, with_dout: Optional[bool] = None, device="cpu") -> 
             x = x * scale
         return x.to(dt)
 
-    q = normal((w.B, w.H, w.N, w.d))
-    k = normal((w.B, w.Hkv, w.N, w.d))
-    v = normal((w.B, w.Hkv, w.N, w.d))
-    alpha = _draw_alpha(gen, (w.B, w.H, w.N), w.alpha)
-    dout = normal((w.B, w.H, w.N, w.d)) if with_dout else None
+    if w.decode:  # the new queries and their gates; k, v are the cache
+        q = normal((w.B, w.H, w.d))
+        k = normal((w.B, w.Hkv, w.N, w.d))
+        v = normal((w.B, w.Hkv, w.N, w.d))
+        alpha = _draw_alpha(gen, (w.B, w.H), w.alpha)
+        dout = None
+    else:
+        q = normal((w.B, w.H, w.N, w.d))
+        k = normal((w.B, w.Hkv, w.N, w.d))
+        v = normal((w.B, w.Hkv, w.N, w.d))
+        alpha = _draw_alpha(gen, (w.B, w.H, w.N), w.alpha)
+        dout = normal((w.B, w.H, w.N, w.d)) if with_dout else None
     out = {"q": q, "k": k, "v": v, "alpha": alpha, "dout": dout}
     if device != "cpu":
         out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
