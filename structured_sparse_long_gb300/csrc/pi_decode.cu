@@ -100,7 +100,8 @@ __device__ __forceinline__ void lds_bf16(const uint8_t *p, float *f) {
     }
 }
 
-template <int D>
+// HPW: query heads per warp, ceil(G / 4) rounded up to 1, 2 or 4 (registers scale with it).
+template <int D, int HPW>
 __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     using L = Lay<D>;
     constexpr int E = D / 32;  // columns per lane
@@ -160,7 +161,6 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     }
 
     // ---- per-warp heads: query slice, prior, online state
-    constexpr int HPW = MAX_G / WARPS;  // at most 4 heads per warp
     float qv[HPW][E], o[HPW][E], m[HPW], l[HPW], offb[HPW], offs[HPW];
 #pragma unroll
     for (int j = 0; j < HPW; ++j) {
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     cluster_sync();  // the other CTAs' shared memory stays alive until CTA 0 has read it
 }
 
-template <int D>
+template <int D, int HPW>
 static cudaError_t launch(const DecArgs &a, int P, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P, (unsigned)a.s.Hkv, (unsigned)a.s.B);
@@ -313,7 +313,7 @@ static cudaError_t launch(const DecArgs &a, int P, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D>, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, HPW>, a);
 }
 
 }  // namespace dec
@@ -346,7 +346,8 @@ cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st) {
     }
     a.n_keys = a.n_band + n_skip;
     a.n_chunks = (a.n_keys + KEYS - 1) / KEYS;
-    // cluster size: enough CTAs for about two per SM, at most one chunk each, at most 8
+    // cluster size: enough CTAs for about two per SM, at most one chunk each, at most 8 (on D4,
+    // 64 sequences x 4 KV heads: 1, 2, 3 and 8 CTAs per cluster ran 31, 25, 29 and 42 us)
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -357,8 +358,17 @@ cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st) {
     const long long pairs = (long long)s.B * s.Hkv;
     int P = (int)std::min<long long>(MAX_P, std::max<long long>(1, (2LL * sms + pairs - 1) / pairs));
     P = std::max(1, std::min(P, a.n_chunks));
-    if (s.d == 64) return launch<64>(a, P, st);
-    if (s.d == 128) return launch<128>(a, P, st);
+    const int hpw = (G + WARPS - 1) / WARPS;
+    if (s.d == 64) {
+        if (hpw <= 1) return launch<64, 1>(a, P, st);
+        if (hpw <= 2) return launch<64, 2>(a, P, st);
+        return launch<64, 4>(a, P, st);
+    }
+    if (s.d == 128) {
+        if (hpw <= 1) return launch<128, 1>(a, P, st);
+        if (hpw <= 2) return launch<128, 2>(a, P, st);
+        return launch<128, 4>(a, P, st);
+    }
     return cudaErrorInvalidValue;
 }
 
