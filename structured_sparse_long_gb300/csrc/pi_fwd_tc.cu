@@ -36,7 +36,12 @@ namespace tc {
 
 constexpr int BM = 128;           // rows per CTA (MMA M)
 constexpr int CHUNK = 32;         // keys per chunk (TMA box rows)
-constexpr int TILE_N = 64;        // keys per tile (2 chunks)
+#ifndef PI_FWD_CPT
+#define PI_FWD_CPT 1
+#endif
+constexpr int CPT = PI_FWD_CPT;   // chunks per key tile (1 or 2)
+constexpr int TILE_N = CPT * CHUNK;
+constexpr int NB = 4 / CPT;       // S buffers: NB x TILE_N = 128 TMEM columns
 constexpr int NUM_THREADS = 256;
 constexpr int TMEM_COLS = 256;    // S buffers [0,128), O [128, 128+d)
 constexpr int O_COL = 128;
@@ -47,27 +52,29 @@ constexpr float kRescaleThreshold = 8.f;      // log2 units
 template <int D>
 struct Cfg {
     static constexpr int KD = D / 64;  // 64-element column blocks of d
-    static constexpr int STAGES = (D == 64) ? 4 : 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_STAGE = TILE_N * D * 2;
+    // 48 KB of K tiles (the S issuer runs furthest ahead) and 32 KB of V tiles
+    static constexpr int KSTAGES = 49152 / KV_STAGE;
+    static constexpr int VSTAGES = 32768 / KV_STAGE;
     static constexpr int KV_DBLK = TILE_N * ROW_BYTES;  // one 64-column block of a stage
     static constexpr int Q_DBLK = BM * ROW_BYTES;
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + Q_BYTES;
-    static constexpr int V_OFF = K_OFF + STAGES * KV_STAGE;
-    static constexpr int DATA_BYTES = V_OFF + STAGES * KV_STAGE;  // from a 1024-byte aligned base
+    static constexpr int V_OFF = K_OFF + KSTAGES * KV_STAGE;
+    static constexpr int DATA_BYTES = V_OFF + VSTAGES * KV_STAGE;  // from a 1024-byte aligned base
     // barrier indices
     static constexpr int B_Q = 0;
     static constexpr int B_KF = 1;
-    static constexpr int B_KE = B_KF + STAGES;
-    static constexpr int B_VF = B_KE + STAGES;
-    static constexpr int B_VE = B_VF + STAGES;
-    static constexpr int B_SF = B_VE + STAGES;  // S of the tile in TMEM buffer t & 1
-    static constexpr int B_PR = B_SF + 2;       // P of the tile written over its S
-    // PV of tile T completes barrier B_PV + (T & 1), phase T >> 1: with two barriers no
-    // parity wait ever has two of its phases outstanding.
-    static constexpr int B_PV = B_PR + 2;
-    static constexpr int B_OF = B_PV + 2;  // O complete (after the last PV), single phase
+    static constexpr int B_KE = B_KF + KSTAGES;
+    static constexpr int B_VF = B_KE + KSTAGES;
+    static constexpr int B_VE = B_VF + VSTAGES;
+    static constexpr int B_SF = B_VE + VSTAGES;  // S of tile t in TMEM buffer t % NB
+    static constexpr int B_PR = B_SF + NB;      // P of the tile written over its S
+    // PV of tile T completes barrier B_PV + T % NB, phase T / NB: a buffer's PV barrier is
+    // waited for in order, so no parity wait has two of its phases outstanding.
+    static constexpr int B_PV = B_PR + NB;
+    static constexpr int B_OF = B_PV + NB;  // O complete (after the last PV), single phase
     static constexpr int B_DR = B_OF + 1;  // drain of the S issuer's MMAs
     static constexpr int B_DR2 = B_DR + 1; // drain of the PV issuer's MMAs
     static constexpr int NBARS = B_DR2 + 1;
@@ -139,13 +146,14 @@ __device__ __forceinline__ float chunk_exp(const float *f, int clo, bool skip, f
 }
 
 // Fast path of a key tile that lies inside the band of every row: P = exp2(f * sc + bo) for
-// the tile's 64 scores, packed as bf16 pairs in place (word c/2 of each chunk, written after
-// scores c and c+1 were read); returns the sum of the fp32 values.
-__device__ __forceinline__ float exp_pack64(uint32_t *ra, uint32_t *rb, float sc, float bo) {
+// the tile's NCH x 32 scores, packed as bf16 pairs in place (word c/2 of each chunk, written
+// after scores c and c+1 were read); returns the sum of the fp32 values.
+template <int NCH>
+__device__ __forceinline__ float exp_pack(uint32_t *ra, uint32_t *rb, float sc, float bo) {
     const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo);
     uint64_t acc[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NCH; ++h) {
         uint32_t *r = h ? rb : ra;
 #pragma unroll
         for (int c = 0; c < CHUNK; c += 2) {
@@ -164,23 +172,26 @@ __device__ __forceinline__ float exp_pack64(uint32_t *ra, uint32_t *rb, float sc
     return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
-// Largest of the 64 raw scores of a tile (eight independent chains).
-__device__ __forceinline__ float max64(const uint32_t *ra, const uint32_t *rb) {
+// Largest of the NCH x 32 raw scores of a tile (four independent chains per chunk).
+template <int NCH>
+__device__ __forceinline__ float max_tile(const uint32_t *ra, const uint32_t *rb) {
     float m[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        m[k] = max3(__uint_as_float(ra[k]), __uint_as_float(ra[k + 4]), __uint_as_float(ra[k + 8]));
-        m[k + 4] = max3(__uint_as_float(rb[k]), __uint_as_float(rb[k + 4]), __uint_as_float(rb[k + 8]));
-    }
+    for (int h = 0; h < NCH; ++h) {
+        const uint32_t *r = h ? rb : ra;
 #pragma unroll
-    for (int c = 12; c < CHUNK; c += 8) {
+        for (int k = 0; k < 4; ++k)
+            m[4 * h + k] = max3(__uint_as_float(r[k]), __uint_as_float(r[k + 4]), __uint_as_float(r[k + 8]));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            m[k] = max3(m[k], __uint_as_float(ra[c + k]), __uint_as_float(ra[c + 4 + k]));
-            m[k + 4] = max3(m[k + 4], __uint_as_float(rb[c + k]), __uint_as_float(rb[c + 4 + k]));
+        for (int c = 12; c < CHUNK; c += 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                m[4 * h + k] = max3(m[4 * h + k], __uint_as_float(r[c + k]), __uint_as_float(r[c + 4 + k]));
         }
     }
-    return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], max3(m[4], m[5], m[6]), m[7]));
+    float mx = fmaxf(max3(m[0], m[1], m[2]), m[3]);
+    if (NCH == 2) mx = fmaxf(mx, fmaxf(max3(m[4], m[5], m[6]), m[7]));
+    return mx;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -241,7 +252,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const TcArgs args) {
     using C = Cfg<D>;
-    constexpr int ST = C::STAGES;
+    constexpr int KST = C::KSTAGES, VST = C::VSTAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -312,7 +323,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
     }
     const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
-    const int n_tiles = (n_chunks + 1) / 2;
+    const int n_tiles = (n_chunks + CPT - 1) / CPT;
     // Band chunks full_lo .. full_hi lie inside the band of every row of the block (the block
     // has no rows past N, the chunk starts at or after the last row's first key and ends at or
     // before the first row): such chunks need no per-row range.
@@ -327,33 +338,34 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ---- setup: barriers, TMEM
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_Q), 1);
-        for (int i = 0; i < ST; ++i) {
+        for (int i = 0; i < KST; ++i) {
             mbar_init(bar(C::B_KF + i), 1);
             mbar_init(bar(C::B_KE + i), 1);
+        }
+        for (int i = 0; i < VST; ++i) {
             mbar_init(bar(C::B_VF + i), 1);
             mbar_init(bar(C::B_VE + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NB; ++i) {
             mbar_init(bar(C::B_SF + i), 1);
             mbar_init(bar(C::B_PR + i), 128);
+            mbar_init(bar(C::B_PV + i), 1);
         }
-        mbar_init(bar(C::B_PV), 1);
-        mbar_init(bar(C::B_PV + 1), 1);
         mbar_init(bar(C::B_OF), 1);
         mbar_init(bar(C::B_DR), 1);
         mbar_init(bar(C::B_DR2), 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    // K and V tile t into ring stage t % ST (the stage must be free)
-    auto issue_kv = [&](const CUtensorMap *tm, uint32_t sbuf, int full_bar, int t, uint64_t policy) {
-        const int st = t % ST;
-        const int nch = min(2, n_chunks - 2 * t);
+    // K or V tile t into stage t % nst of its ring (the stage must be free)
+    auto issue_kv = [&](const CUtensorMap *tm, uint32_t sbuf, int full_bar, int nst, int t, uint64_t policy) {
+        const int st = t % nst;
+        const int nch = min(CPT, n_chunks - CPT * t);
         mbar_expect_tx(bar(full_bar + st), nch * C::KD * BOX_BYTES);
         for (int cc = 0; cc < nch; ++cc) {
             int back, u;
             bool sk;
-            const int key0 = cw.key0(2 * t + cc, back, u, sk);
+            const int key0 = cw.key0(CPT * t + cc, back, u, sk);
             for (int dc = 0; dc < C::KD; ++dc)
                 tma_load_3d_hint(sbuf + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, tm, dc * 64,
                                  key0, b * s.Hkv + g, bar(full_bar + st), policy);
@@ -370,7 +382,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                              policy_evict_first());
         stamp(2);
         stamp_tile(8, 0);
-        issue_kv(&tmK, sK, C::B_KF, 0, policy_evict_last());
+        issue_kv(&tmK, sK, C::B_KF, KST, 0, policy_evict_last());
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
@@ -388,18 +400,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const uint64_t reused = policy_evict_last();
             int issued = 1;
             for (int t = 1; t < n_tiles; ++t) {
-                const int st = t % ST, round = t / ST;
+                const int st = t % KST, round = t / KST;
                 if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
                 stamp_tile(8, t);
-                issue_kv(&tmK, sK, C::B_KF, t, reused);
+                issue_kv(&tmK, sK, C::B_KF, KST, t, reused);
                 issued = t + 1;
             }
             if (*abort_flag) {  // let loads in flight land before the CTA leaves
                 volatile uint32_t zero = 0;
                 WaitCtx w2{&zero, nullptr, 20000000ull};
                 wait_bar(bar(C::B_Q), 0, w2);
-                for (int t = max(0, issued - ST); t < issued; ++t)
-                    wait_bar(bar(C::B_KF + t % ST), (t / ST) & 1, w2);
+                for (int t = max(0, issued - KST); t < issued; ++t)
+                    wait_bar(bar(C::B_KF + t % KST), (t / KST) & 1, w2);
             }
         }
     } else if (warp == 2) {
@@ -409,17 +421,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const uint64_t reused = policy_evict_last();
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
-                const int st = t % ST, round = t / ST;
+                const int st = t % VST, round = t / VST;
                 if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
                 stamp_tile(24, t);
-                issue_kv(&tmV, sV, C::B_VF, t, reused);
+                issue_kv(&tmV, sV, C::B_VF, VST, t, reused);
                 issued = t + 1;
             }
             if (*abort_flag) {
                 volatile uint32_t zero = 0;
                 WaitCtx w2{&zero, nullptr, 20000000ull};
-                for (int t = max(0, issued - ST); t < issued; ++t)
-                    wait_bar(bar(C::B_VF + t % ST), (t / ST) & 1, w2);
+                for (int t = max(0, issued - VST); t < issued; ++t)
+                    wait_bar(bar(C::B_VF + t % VST), (t / VST) & 1, w2);
             }
         }
     } else if (warp == 1) {
@@ -429,12 +441,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             bool ok = wait_bar(bar(C::B_Q), 0, wc);
             if (ok) stamp(3);
             for (int t = 0; ok && t < n_tiles; ++t) {
-                const int st = t % ST, buf = t & 1;
-                if (!timed_wait(bar(C::B_KF + st), (t / ST) & 1, 104, t)) break;
-                // buffer buf last held P of tile t-2: its PV must be done
-                if (t >= 2 && !timed_wait(bar(C::B_PV + buf), ((t - 2) >> 1) & 1, 120, t)) break;
+                const int st = t % KST, buf = t % NB;
+                if (!timed_wait(bar(C::B_KF + st), (t / KST) & 1, 104, t)) break;
+                // buffer buf last held P of tile t-NB: its PV must be done
+                if (t >= NB && !timed_wait(bar(C::B_PV + buf), ((t - NB) / NB) & 1, 120, t)) break;
                 tc_fence_after();
-                const int nch = min(2, n_chunks - 2 * t);
+                const int nch = min(CPT, n_chunks - CPT * t);
                 const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
                 const uint32_t dS = tbase + buf * TILE_N;
 #pragma unroll
@@ -462,11 +474,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) {
             bool ok = true;
             for (int u = 0; ok && u < n_tiles; ++u) {
-                const int st = u % ST, buf = u & 1;
-                if (!timed_wait(bar(C::B_PR + buf), (u >> 1) & 1, 136, u)) break;
-                if (!timed_wait(bar(C::B_VF + st), (u / ST) & 1, 152, u)) break;
+                const int st = u % VST, buf = u % NB;
+                if (!timed_wait(bar(C::B_PR + buf), (u / NB) & 1, 136, u)) break;
+                if (!timed_wait(bar(C::B_VF + st), (u / VST) & 1, 152, u)) break;
                 tc_fence_after();
-                const int nch = min(2, n_chunks - 2 * u);
+                const int nch = min(CPT, n_chunks - CPT * u);
                 const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
                 const uint32_t aP = tbase + buf * TILE_N;
                 for (int kk = 0; kk < 2 * nch; ++kk) {
@@ -529,7 +541,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // and PV of tile t+1 cannot start before this thread arrives for tile t+1.
         auto rescale_o = [&](int t, bool need_o, float corr) -> bool {
             if (!__any_sync(0xffffffffu, need_o)) return true;
-            const bool r_ = wait_bar(bar(C::B_PV + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc);
+            const bool r_ = wait_bar(bar(C::B_PV + (t - 1) % NB), ((t - 1) / NB) & 1, wc);
             if (!__all_sync(0xffffffffu, r_)) return false;
             tc_fence_after();
             const float f = need_o ? corr : 1.f;
@@ -546,15 +558,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         };
 
         for (int t = 0; t < n_tiles; ++t) {
-            const int buf = t & 1;
-            if (warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (t >> 1) & 1, 168, t);
-            else ok = wait_bar(bar(C::B_SF + buf), (t >> 1) & 1, wc);
+            const int buf = t % NB;
+            if (warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (t / NB) & 1, 168, t);
+            else ok = wait_bar(bar(C::B_SF + buf), (t / NB) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             if (warp == 4 && lane == 0) stamp_tile(72, t);
             tc_fence_after();
             __syncwarp();
-            const int nch = min(2, n_chunks - 2 * t);
+            const int nch = (CPT == 1) ? 1 : min(2, n_chunks - 2 * t);
             const uint32_t tS = tbase + lane_base + buf * TILE_N;
             uint32_t ra[CHUNK], rb[CHUNK];
             tmem_ld32(tS, ra);
@@ -566,35 +578,35 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // maximum is only needed when some P exceeds 2^8 (the lazy-rescale bound), which a
             // sum above 2^8 is the first sign of.  Rows with no reference yet take the general
             // path, as do the debug modes that record per-row ranges.
-            const bool fast = (DBG == 0 || DBG == 3) && nch == 2 && 2 * t >= full_lo && 2 * t + 1 <= full_hi &&
-                              __all_sync(0xffffffffu, m_ref != -INFINITY);
+            const bool fast = (DBG == 0 || DBG == 3) && nch == CPT && CPT * t >= full_lo &&
+                              CPT * t + CPT - 1 <= full_hi && __all_sync(0xffffffffu, m_ref != -INFINITY);
             float corr = 1.f, lsum;
             bool need_o = false;
             if (fast) {
-                lsum = exp_pack64(ra, rb, sc, off_band - m_ref);
+                lsum = exp_pack<CPT>(ra, rb, sc, off_band - m_ref);
                 if (__any_sync(0xffffffffu, !(lsum <= 256.f))) {
                     tmem_ld32(tS, ra);  // S is still in TMEM: P has not been written yet
-                    tmem_ld32(tS + CHUNK, rb);
+                    if (CPT == 2) tmem_ld32(tS + CHUNK, rb);
                     tmem_wait_ld();
-                    const float mt = fmaf(max64(ra, rb), sc, off_band);
+                    const float mt = fmaf(max_tile<CPT>(ra, rb), sc, off_band);
                     if (mt > m_ref + kRescaleThreshold) {
                         corr = fast_exp2(m_ref - mt);
                         need_o = true;  // m_ref was set by an earlier tile, so t > 0
                         m_ref = mt;
                     }
                     l *= corr;
-                    lsum = exp_pack64(ra, rb, sc, off_band - m_ref);
+                    lsum = exp_pack<CPT>(ra, rb, sc, off_band - m_ref);
                 }
                 if (warp == 4 && lane == 0) stamp_tile(200, t);
                 tmem_st16(tS, ra);
-                tmem_st16(tS + CHUNK / 2, rb);
+                if (CPT == 2) tmem_st16(tS + CHUNK / 2, rb);
             } else {
 
                 int key0a, cloa, chia, key0b = 0, clob = CHUNK, chib = -1;
                 float offa, offb = 0.f;
                 bool ska, skb = false;
-                chunk_range(2 * t, key0a, cloa, chia, offa, ska);
-                if (nch > 1) chunk_range(2 * t + 1, key0b, clob, chib, offb, skb);
+                chunk_range(CPT * t, key0a, cloa, chia, offa, ska);
+                if (nch > 1) chunk_range(CPT * t + 1, key0b, clob, chib, offb, skb);
 
                 float *fa = reinterpret_cast<float *>(ra);
                 float *fb = reinterpret_cast<float *>(rb);
