@@ -335,27 +335,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         full_hi = span >= 0 ? min(span / CHUNK, cw.n_band - 1) : -1;
     }
 
-    // ---- setup: barriers, TMEM
-    if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_Q), 1);
-        for (int i = 0; i < KST; ++i) {
-            mbar_init(bar(C::B_KF + i), 1);
-            mbar_init(bar(C::B_KE + i), 1);
-        }
-        for (int i = 0; i < VST; ++i) {
-            mbar_init(bar(C::B_VF + i), 1);
-            mbar_init(bar(C::B_VE + i), 1);
-        }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(bar(C::B_SF + i), 1);
-            mbar_init(bar(C::B_PR + i), 128);
-            mbar_init(bar(C::B_PV + i), 1);
-        }
-        mbar_init(bar(C::B_OF), 1);
-        mbar_init(bar(C::B_DR), 1);
-        mbar_init(bar(C::B_DR2), 1);
-        *abort_flag = 0u;
+    // ---- setup: barriers (spread over warp 0's lanes; only the P-ready barriers count 128
+    // arrivals), TMEM
+    if (warp == 0) {
+        for (int idx = lane; idx < C::NBARS; idx += 32)
+            mbar_init(bar(idx), (idx >= C::B_PR && idx < C::B_PR + NB) ? 128u : 1u);
+        if (lane == 0) *abort_flag = 0u;
         fence_barrier_init();
+        __syncwarp();
     }
     // K or V tile t into stage t % nst of its ring (the stage must be free)
     auto issue_kv = [&](const CUtensorMap *tm, uint32_t sbuf, int full_bar, int nst, int t, uint64_t policy) {
