@@ -35,7 +35,6 @@ using namespace tc;
 
 constexpr int BM = 128;     // rows per CTA (MMA M)
 constexpr int CHUNK = 32;   // keys per chunk (TMA box rows)
-constexpr int TILE_N = 64;  // keys per tile
 constexpr int NUM_THREADS = 256;
 constexpr int ROW_BYTES = 128;
 constexpr int BOX_BYTES = CHUNK * ROW_BYTES;
@@ -77,11 +76,13 @@ struct QWalk {
 template <int D>
 struct CfgQ {
     static constexpr int KD = D / 64;
-    static constexpr int ST = (D == 64) ? 4 : 2;
+    static constexpr int CPT = (D == 64) ? 1 : 2;  // chunks per key tile
+    static constexpr int TILE = CPT * CHUNK;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int Q_DBLK = BM * ROW_BYTES;
-    static constexpr int KV_STAGE = TILE_N * D * 2;
-    static constexpr int KV_DBLK = TILE_N * ROW_BYTES;
+    static constexpr int KV_STAGE = TILE * D * 2;
+    static constexpr int KV_DBLK = TILE * ROW_BYTES;
+    static constexpr int ST = 32768 / KV_STAGE;  // 32 KB of K tiles and 32 KB of V tiles
     static constexpr int Q_OFF = 0;
     static constexpr int G_OFF = Q_BYTES;  // dO tile
     static constexpr int K_OFF = 2 * Q_BYTES;
@@ -92,15 +93,19 @@ struct CfgQ {
     static constexpr int B_KE = B_KF + ST;
     static constexpr int B_VF = B_KE + ST;
     static constexpr int B_VE = B_VF + ST;
-    static constexpr int B_SF = B_VE + ST;  // S and dP of the tile in TMEM
-    static constexpr int B_PR = B_SF + 1;   // p and p*dp written back (128 arrivals)
-    static constexpr int B_BF = B_PR + 1;   // A1/A2 MMAs of the tile done: S/dP columns free
-    static constexpr int B_AF = B_BF + 1;   // A1/A2 complete (single phase)
-    static constexpr int B_DR = B_AF + 1;
-    static constexpr int NBARS = B_DR + 1;
+    // Two S/dP buffers in TMEM: tile t uses buffer t & 1.  Per buffer: S and dP written by the
+    // MMAs, then p (dp - c) and p written back over them for the A1/A2 MMAs.
+    static constexpr int B_SF = B_VE + ST;  // [2] S and dP of the tile in TMEM
+    static constexpr int B_PR = B_SF + 2;   // [2] p and p (dp - c) written back (128 arrivals)
+    static constexpr int B_BF = B_PR + 2;   // [2] A1/A2 MMAs of the tile done: buffer free
+    static constexpr int B_AF = B_BF + 2;   // A1/A2 complete (single phase)
+    static constexpr int B_DR = B_AF + 1;   // drain of the S/dP issuer
+    static constexpr int B_DR2 = B_DR + 1;  // drain of the A1/A2 issuer
+    static constexpr int NBARS = B_DR2 + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
     // TMEM columns
-    static constexpr int S_COL = 0, DP_COL = 64, A1_COL = 128, A2_COL = 128 + D;
+    static constexpr int BUF = 2 * TILE;  // S then dP of one buffer
+    static constexpr int S_COL = 0, DP_COL = TILE, A1_COL = 2 * BUF, A2_COL = 2 * BUF + D;
     static constexpr int TMEM_COLS = (A2_COL + D <= 256) ? 256 : 512;
 };
 
@@ -167,23 +172,15 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         n_skip_blocks = max(0, m_last - cw.m_first + 1);
     }
     const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
-    const int n_tiles = (n_chunks + 1) / 2;
+    constexpr int CPT = C::CPT;
+    const int n_tiles = (n_chunks + CPT - 1) / CPT;
 
-    if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_QF), 1);
-        for (int i = 0; i < ST; ++i) {
-            mbar_init(bar(C::B_KF + i), 1);
-            mbar_init(bar(C::B_KE + i), 1);
-            mbar_init(bar(C::B_VF + i), 1);
-            mbar_init(bar(C::B_VE + i), 1);
-        }
-        mbar_init(bar(C::B_SF), 1);
-        mbar_init(bar(C::B_PR), 128);
-        mbar_init(bar(C::B_BF), 1);
-        mbar_init(bar(C::B_AF), 1);
-        mbar_init(bar(C::B_DR), 1);
-        *abort_flag = 0u;
+    if (warp == 0) {  // barriers spread over warp 0's lanes; only the P-ready ones count 128
+        for (int idx = lane; idx < C::NBARS; idx += 32)
+            mbar_init(bar(idx), (idx == C::B_PR || idx == C::B_PR + 1) ? 128u : 1u);
+        if (lane == 0) *abort_flag = 0u;
         fence_barrier_init();
+        __syncwarp();
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tc_fence_before();
@@ -207,12 +204,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) break;
-                const int nch = min(2, n_chunks - 2 * t);
+                const int nch = min(CPT, n_chunks - CPT * t);
                 mbar_expect_tx(bar(C::B_KF + st), nch * C::KD * BOX_BYTES);
                 for (int cc = 0; cc < nch; ++cc) {
                     int back;
                     bool sk;
-                    const int key0 = cw.key0(2 * t + cc, back, sk);
+                    const int key0 = cw.key0(CPT * t + cc, back, sk);
                     for (int dc = 0; dc < C::KD; ++dc)
                         tma_load_3d_hint(sK + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmK,
                                          dc * 64, key0, b * s.Hkv + g, bar(C::B_KF + st), reused);
@@ -236,12 +233,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % ST, round = t / ST;
                 if (round > 0 && !wait_bar(bar(C::B_VE + st), (round - 1) & 1, wc)) break;
-                const int nch = min(2, n_chunks - 2 * t);
+                const int nch = min(CPT, n_chunks - CPT * t);
                 mbar_expect_tx(bar(C::B_VF + st), nch * C::KD * BOX_BYTES);
                 for (int cc = 0; cc < nch; ++cc) {
                     int back;
                     bool sk;
-                    const int key0 = cw.key0(2 * t + cc, back, sk);
+                    const int key0 = cw.key0(CPT * t + cc, back, sk);
                     for (int dc = 0; dc < C::KD; ++dc)
                         tma_load_3d_hint(sV + st * C::KV_STAGE + dc * C::KV_DBLK + cc * BOX_BYTES, &tmV,
                                          dc * 64, key0, b * s.Hkv + g, bar(C::B_VF + st), reused);
@@ -256,50 +253,65 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
         }
     } else if (warp == 1) {
-        // ================= MMA issuer
+        // ================= S/dP issuer: S = Q K^T and dP = dO V^T into buffer t & 1, as soon as
+        // that buffer's previous A1/A2 MMAs (tile t-2) are done
         if (lane == 0) {
             bool ok = wait_bar(bar(C::B_QF), 0, wc);
             for (int t = 0; ok && t < n_tiles; ++t) {
-                const int st = t % ST;
+                const int st = t % ST, buf = t & 1;
                 if (!wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc)) break;
                 if (!wait_bar(bar(C::B_VF + st), (t / ST) & 1, wc)) break;
-                // the S/dP columns still hold the operands of tile t-1's A1/A2 MMAs
-                if (t >= 1 && !wait_bar(bar(C::B_BF), (t - 1) & 1, wc)) break;
+                if (t >= 2 && !wait_bar(bar(C::B_BF + buf), ((t - 2) >> 1) & 1, wc)) break;
                 tc_fence_after();
-                const int nch = min(2, n_chunks - 2 * t);
+                const int nch = min(CPT, n_chunks - CPT * t);
                 const uint32_t idesc_s = idesc_bf16(BM, CHUNK * nch, 0, 0);
+                const uint32_t dS = tbase + C::S_COL + buf * C::BUF, dP = tbase + C::DP_COL + buf * C::BUF;
 #pragma unroll
                 for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (dc | ks) != 0;
-                        mma_ss(tbase + C::S_COL, sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024),
+                        mma_ss(dS, sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024),
                                sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
                                idesc_s, acc);
-                        mma_ss(tbase + C::DP_COL, sdesc(sG + dc * C::Q_DBLK + ks * 32, 16, 1024),
+                        mma_ss(dP, sdesc(sG + dc * C::Q_DBLK + ks * 32, 16, 1024),
                                sdesc(sV + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
                                idesc_s, acc);
                     }
                 }
-                tc_commit(bar(C::B_SF));
-                tc_commit(bar(C::B_VE + st));
-                if (!wait_bar(bar(C::B_PR), t & 1, wc)) break;
-                tc_fence_after();
-                const uint32_t idesc_a = idesc_bf16(BM, D, 0, 1);
-                for (int kk = 0; kk < 2 * nch; ++kk) {
-                    const uint64_t kb = sdesc(sK + st * C::KV_STAGE + kk * 16 * ROW_BYTES, C::KV_DBLK, 1024);
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tbase + C::A1_COL, tbase + C::S_COL + kk * 8, kb, idesc_a, acc);
-                    mma_ts(tbase + C::A2_COL, tbase + C::DP_COL + kk * 8, kb, idesc_a, acc);
-                }
-                tc_commit(bar(C::B_BF));
-                tc_commit(bar(C::B_KE + st));
-                if (t == n_tiles - 1) tc_commit(bar(C::B_AF));
+                tc_commit(bar(C::B_SF + buf));
+                tc_commit(bar(C::B_VE + st));  // V is read by dP only
             }
             tc_commit(bar(C::B_DR));
             volatile uint32_t zero = 0;
             WaitCtx w2{&zero, args.status, args.timeout_ns};
             wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp == 3) {
+        // ================= A1/A2 issuer: A1 += p (dp - c) K, A2 += p K from buffer t & 1
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t idesc_a = idesc_bf16(BM, D, 0, 1);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int st = t % ST, buf = t & 1;
+                // K of tile t landed before S of tile t, which the softmax saw before P
+                if (!wait_bar(bar(C::B_PR + buf), (t >> 1) & 1, wc)) break;
+                tc_fence_after();
+                const int nch = min(CPT, n_chunks - CPT * t);
+                for (int kk = 0; kk < 2 * nch; ++kk) {
+                    const uint64_t kb = sdesc(sK + st * C::KV_STAGE + kk * 16 * ROW_BYTES, C::KV_DBLK, 1024);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tbase + C::A1_COL, tbase + C::S_COL + buf * C::BUF + kk * 8, kb, idesc_a, acc);
+                    mma_ts(tbase + C::A2_COL, tbase + C::DP_COL + buf * C::BUF + kk * 8, kb, idesc_a, acc);
+                }
+                tc_commit(bar(C::B_BF + buf));
+                tc_commit(bar(C::B_KE + st));  // K is read by S and by A1/A2, which come last
+                if (t == n_tiles - 1) tc_commit(bar(C::B_AF));
+            }
+            tc_commit(bar(C::B_DR2));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR2), 0, w2);
         }
     } else if (warp >= 4) {
         // ================= one thread per query row
@@ -341,16 +353,18 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
 
         for (int t = 0; t < n_tiles; ++t) {
-            ok = wait_bar(bar(C::B_SF), t & 1, wc);
+            const int buf = t & 1;
+            const uint32_t bcol = tbase + lane_base + buf * C::BUF;
+            ok = wait_bar(bar(C::B_SF + buf), (t >> 1) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             __syncwarp();
-            const int nch = min(2, n_chunks - 2 * t);
+            const int nch = min(CPT, n_chunks - CPT * t);
             for (int cc = 0; cc < nch; ++cc) {
                 int back;
                 bool sk;
-                const int key0 = cw.key0(2 * t + cc, back, sk);
+                const int key0 = cw.key0(CPT * t + cc, back, sk);
                 int clo, chi;
                 float off;
                 if (!sk) {
@@ -369,8 +383,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t sr[16], dr[16];
-                    tmem_ld16(tbase + lane_base + C::S_COL + cc * CHUNK + half * 16, sr);
-                    tmem_ld16(tbase + lane_base + C::DP_COL + cc * CHUNK + half * 16, dr);
+                    tmem_ld16(bcol + C::S_COL + cc * CHUNK + half * 16, sr);
+                    tmem_ld16(bcol + C::DP_COL + cc * CHUNK + half * 16, dr);
                     tmem_wait_ld();
                     uint32_t pw[8], pp[8];
 #pragma unroll
@@ -391,13 +405,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     }
                     // A1 operand p (dp - c) over the S columns, A2 operand p over the dP columns;
                     // both chunk halves' values are already in registers
-                    tmem_st8(tbase + lane_base + C::S_COL + cc * (CHUNK / 2) + half * 8, pw);
-                    tmem_st8(tbase + lane_base + C::DP_COL + cc * (CHUNK / 2) + half * 8, pp);
+                    tmem_st8(bcol + C::S_COL + cc * (CHUNK / 2) + half * 8, pw);
+                    tmem_st8(bcol + C::DP_COL + cc * (CHUNK / 2) + half * 8, pp);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PR));
+            mbar_arrive(bar(C::B_PR + buf));
         }
 
         // ---- epilogue: dq = tau (A1 - (D - c) A2) -> bf16 -> shared (Q buffer) -> TMA store
