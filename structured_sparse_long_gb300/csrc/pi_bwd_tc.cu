@@ -495,26 +495,25 @@ static cudaError_t launch_dq(const CUtensorMap &mq, const CUtensorMap &mg, const
 
 // ---------------------------------------------------------------------------- kernel 2
 
-constexpr int QC = 64;      // queries per chunk (N of the transposed MMAs)
 constexpr int BK = 128;     // keys per CTA (M)
 
-// The query chunks that attend to keys [j0, j0 + 128) of one KV head, for one query head:
-// band chunks i0 = j0 + 64c up to the last query whose band holds key j0 + 127, then two
-// chunks per skip multiple m (queries j0 + m*period + [0, 128)).
+// The query chunks (qc queries each) that attend to keys [j0, j0 + 128) of one KV head, for
+// one query head: band chunks i0 = j0 + qc*c up to the last query whose band holds key
+// j0 + 127, then 128/qc chunks per skip multiple m (queries j0 + m*period + [0, 128)).
 struct KWalk {
-    int j0, n_band, m_first, n_skip, period, per_head;
+    int j0, n_band, m_first, n_skip, period, per_head, qc, cps_log2;
     __device__ __forceinline__ void chunk(int ci, int &hh, int &i0, int &back, bool &skip) const {
         hh = ci / per_head;
         const int c = ci - hh * per_head;
         if (c < n_band) {
-            i0 = j0 + c * QC;
+            i0 = j0 + c * qc;
             back = 0;
             skip = false;
         } else {
             const int sc = c - n_band;
-            const int m = m_first + (sc >> 1);
+            const int m = m_first + (sc >> cps_log2);
             back = m * period;
-            i0 = j0 + back + (sc & 1) * QC;
+            i0 = j0 + back + (sc & ((1 << cps_log2) - 1)) * qc;
             skip = true;
         }
     }
@@ -523,7 +522,9 @@ struct KWalk {
 template <int D>
 struct CfgK {
     static constexpr int KD = D / 64;
-    static constexpr int ST = 3;  // query-chunk stages
+    static constexpr int QC = (D == 64) ? 32 : 64;  // queries per chunk (N of the transposed MMAs)
+    static constexpr int CPS_LOG2 = (D == 64) ? 2 : 1;  // log2(BK / QC): chunks per skip block
+    static constexpr int ST = (D == 64) ? 6 : 3;        // query-chunk stages
     static constexpr int KT_BYTES = BK * D * 2;
     static constexpr int KT_DBLK = BK * ROW_BYTES;
     static constexpr int QC_BYTES = QC * D * 2;
@@ -539,14 +540,17 @@ struct CfgK {
     static constexpr int B_QE = B_QF + ST;         // [ST] chunk consumed by its dV/dK MMAs
     static constexpr int B_XF = B_QE + ST;         // [ST] per-query vectors ready (32 arrivals)
     static constexpr int B_XE = B_XF + ST;         // [ST] vectors consumed (128 arrivals)
-    static constexpr int B_SF = B_XE + ST;         // S^T, dP^T in TMEM
-    static constexpr int B_PR = B_SF + 1;          // P^T, dZ^T written back (128 arrivals)
-    static constexpr int B_BF = B_PR + 1;          // dV/dK MMAs of the chunk done
-    static constexpr int B_OF = B_BF + 1;          // dK, dV complete (single phase)
-    static constexpr int B_DR = B_OF + 1;
-    static constexpr int NBARS = B_DR + 1;
+    // Two S^T/dP^T buffers in TMEM: chunk ci uses buffer ci & 1.
+    static constexpr int B_SF = B_XE + ST;         // [2] S^T, dP^T in TMEM
+    static constexpr int B_PR = B_SF + 2;          // [2] P^T, dZ^T written back (128 arrivals)
+    static constexpr int B_BF = B_PR + 2;          // [2] dV/dK MMAs of the chunk done: buffer free
+    static constexpr int B_OF = B_BF + 2;          // dK, dV complete (single phase)
+    static constexpr int B_DR = B_OF + 1;          // drain of the S^T/dP^T issuer
+    static constexpr int B_DR2 = B_DR + 1;         // drain of the dV/dK issuer
+    static constexpr int NBARS = B_DR2 + 1;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
-    static constexpr int ST_COL = 0, DPT_COL = 64, DV_COL = 128, DK_COL = 128 + D;
+    static constexpr int BUF = 2 * QC;  // S^T then dP^T of one buffer
+    static constexpr int ST_COL = 0, DPT_COL = QC, DV_COL = 2 * BUF, DK_COL = 2 * BUF + D;
     static constexpr int TMEM_COLS = (DK_COL + D <= 256) ? 256 : 512;
 };
 
@@ -567,6 +571,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                    const DkvArgs args) {
     using C = CfgK<D>;
     constexpr int ST = C::ST;
+    constexpr int QC = C::QC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -593,6 +598,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     KWalk kw;
     kw.j0 = kb * BK;
     kw.period = s.period;
+    kw.qc = QC;
+    kw.cps_log2 = C::CPS_LOG2;
     const int qlast = band_last_query(min(s.N - 1, kw.j0 + BK - 1), s.N, s.mode, s.k_local);
     kw.n_band = (qlast - kw.j0) / QC + 1;
     kw.m_first = 1;
@@ -601,26 +608,21 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         kw.m_first = max(1, s.k_local / s.period + 1);
         // multiples whose first skip query is inside the sequence
         const int m_last = min(s.S, (s.N - 1 - kw.j0) / s.period);
-        kw.n_skip = 2 * max(0, m_last - kw.m_first + 1);
+        kw.n_skip = (1 << C::CPS_LOG2) * max(0, m_last - kw.m_first + 1);
     }
     kw.per_head = kw.n_band + kw.n_skip;
     const int n_chunks = G * kw.per_head;
 
-    if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_KV), 1);
-        for (int i = 0; i < ST; ++i) {
-            mbar_init(bar(C::B_QF + i), 1);
-            mbar_init(bar(C::B_QE + i), 1);
-            mbar_init(bar(C::B_XF + i), 32);
-            mbar_init(bar(C::B_XE + i), 128);
+    if (warp == 0) {  // barriers spread over warp 0's lanes
+        for (int idx = lane; idx < C::NBARS; idx += 32) {
+            uint32_t count = 1;
+            if (idx >= C::B_XF && idx < C::B_XF + ST) count = 32;
+            if ((idx >= C::B_XE && idx < C::B_XE + ST) || idx == C::B_PR || idx == C::B_PR + 1) count = 128;
+            mbar_init(bar(idx), count);
         }
-        mbar_init(bar(C::B_SF), 1);
-        mbar_init(bar(C::B_PR), 128);
-        mbar_init(bar(C::B_BF), 1);
-        mbar_init(bar(C::B_OF), 1);
-        mbar_init(bar(C::B_DR), 1);
-        *abort_flag = 0u;
+        if (lane == 0) *abort_flag = 0u;
         fence_barrier_init();
+        __syncwarp();
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tc_fence_before();
@@ -682,7 +684,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const long long rbase = ((long long)b * s.H + g * G + hh) * s.N;
             float *xb = xvec + st * 2 * QC;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
+            for (int e = 0; e < QC / 32; ++e) {
                 const int c = lane + 32 * e, i = i0 + c;
                 float bias = -INFINITY, dv = 0.f;
                 if (i < s.N) {
@@ -698,48 +700,63 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             mbar_arrive(bar(C::B_XF + st));
         }
     } else if (warp == 1) {
-        // ================= MMA issuer
+        // ================= S^T/dP^T issuer: into buffer ci & 1 once its previous dV/dK MMAs
+        // (chunk ci-2) are done
         if (lane == 0) {
             bool ok = wait_bar(bar(C::B_KV), 0, wc);
             const uint32_t idesc_t = idesc_bf16(BK, QC, 0, 0);  // S^T, dP^T: both operands K-major
-            const uint32_t idesc_a = idesc_bf16(BK, D, 0, 1);   // dV, dK: B = chunk, MN-major
             for (int ci = 0; ok && ci < n_chunks; ++ci) {
-                const int st = ci % ST;
+                const int st = ci % ST, buf = ci & 1;
                 if (!wait_bar(bar(C::B_QF + st), (ci / ST) & 1, wc)) break;
-                // S^T / dP^T columns still hold the operands of chunk ci-1's dV/dK MMAs
-                if (ci >= 1 && !wait_bar(bar(C::B_BF), (ci - 1) & 1, wc)) break;
+                if (ci >= 2 && !wait_bar(bar(C::B_BF + buf), ((ci - 2) >> 1) & 1, wc)) break;
                 tc_fence_after();
                 const uint32_t q_st = sQ + st * C::QC_BYTES, g_st = sG + st * C::QC_BYTES;
+                const uint32_t dS = tbase + C::ST_COL + buf * C::BUF, dP = tbase + C::DPT_COL + buf * C::BUF;
 #pragma unroll
                 for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (dc | ks) != 0;
-                        mma_ss(tbase + C::ST_COL, sdesc(sK + dc * C::KT_DBLK + ks * 32, 16, 1024),
+                        mma_ss(dS, sdesc(sK + dc * C::KT_DBLK + ks * 32, 16, 1024),
                                sdesc(q_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
-                        mma_ss(tbase + C::DPT_COL, sdesc(sV + dc * C::KT_DBLK + ks * 32, 16, 1024),
+                        mma_ss(dP, sdesc(sV + dc * C::KT_DBLK + ks * 32, 16, 1024),
                                sdesc(g_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
                     }
                 }
-                tc_commit(bar(C::B_SF));
-                if (!wait_bar(bar(C::B_PR), ci & 1, wc)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < QC / 16; ++kk) {
-                    const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tbase + C::DV_COL, tbase + C::ST_COL + kk * 8,
-                           sdesc(g_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
-                    mma_ts(tbase + C::DK_COL, tbase + C::DPT_COL + kk * 8,
-                           sdesc(q_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
-                }
-                tc_commit(bar(C::B_BF));
-                tc_commit(bar(C::B_QE + st));
-                if (ci == n_chunks - 1) tc_commit(bar(C::B_OF));
+                tc_commit(bar(C::B_SF + buf));
             }
             tc_commit(bar(C::B_DR));
             volatile uint32_t zero = 0;
             WaitCtx w2{&zero, args.status, args.timeout_ns};
             wait_bar(bar(C::B_DR), 0, w2);
+        }
+    } else if (warp == 3) {
+        // ================= dV/dK issuer: dV += P^T dO, dK += dZ^T Q from buffer ci & 1
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t idesc_a = idesc_bf16(BK, D, 0, 1);   // dV, dK: B = chunk, MN-major
+            for (int ci = 0; ok && ci < n_chunks; ++ci) {
+                const int st = ci % ST, buf = ci & 1;
+                // the chunk's Q/dO landed before its S^T, which the key threads saw before P^T
+                if (!wait_bar(bar(C::B_PR + buf), (ci >> 1) & 1, wc)) break;
+                tc_fence_after();
+                const uint32_t q_st = sQ + st * C::QC_BYTES, g_st = sG + st * C::QC_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < QC / 16; ++kk) {
+                    const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tbase + C::DV_COL, tbase + C::ST_COL + buf * C::BUF + kk * 8,
+                           sdesc(g_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
+                    mma_ts(tbase + C::DK_COL, tbase + C::DPT_COL + buf * C::BUF + kk * 8,
+                           sdesc(q_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
+                }
+                tc_commit(bar(C::B_BF + buf));
+                tc_commit(bar(C::B_QE + st));
+                if (ci == n_chunks - 1) tc_commit(bar(C::B_OF));
+            }
+            tc_commit(bar(C::B_DR2));
+            volatile uint32_t zero = 0;
+            WaitCtx w2{&zero, args.status, args.timeout_ns};
+            wait_bar(bar(C::B_DR2), 0, w2);
         }
     } else if (warp >= 4) {
         // ================= one thread per key
@@ -753,8 +770,9 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         bool ok = true;
 
         for (int ci = 0; ci < n_chunks; ++ci) {
-            const int st = ci % ST;
-            ok = wait_bar(bar(C::B_SF), ci & 1, wc);
+            const int st = ci % ST, buf = ci & 1;
+            const uint32_t bcol = tbase + lane_base + buf * C::BUF;
+            ok = wait_bar(bar(C::B_SF + buf), (ci >> 1) & 1, wc);
             ok = ok && wait_bar(bar(C::B_XF + st), (ci / ST) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -778,8 +796,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
             for (int q = 0; q < QC / 16; ++q) {
                 uint32_t sr[16], dr[16];
-                tmem_ld16(tbase + lane_base + C::ST_COL + q * 16, sr);
-                tmem_ld16(tbase + lane_base + C::DPT_COL + q * 16, dr);
+                tmem_ld16(bcol + C::ST_COL + q * 16, sr);
+                tmem_ld16(bcol + C::DPT_COL + q * 16, dr);
                 tmem_wait_ld();
                 uint32_t pp[8], pz[8];
 #pragma unroll
@@ -795,12 +813,12 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     pp[c / 2] = pack_bf16(p0, p1);
                     pz[c / 2] = pack_bf16(z0, z1);
                 }
-                tmem_st8(tbase + lane_base + C::ST_COL + q * 8, pp);
-                tmem_st8(tbase + lane_base + C::DPT_COL + q * 8, pz);
+                tmem_st8(bcol + C::ST_COL + q * 8, pp);
+                tmem_st8(bcol + C::DPT_COL + q * 8, pz);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PR));
+            mbar_arrive(bar(C::B_PR + buf));
             mbar_arrive(bar(C::B_XE + st));
         }
 
@@ -907,8 +925,8 @@ cudaError_t launch_bwd_dkdv_tc(const LaunchBwd &L, int *status, uint64_t timeout
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
         !make_map(&mdk, L.dk, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
         !make_map(&mdv, L.dv, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
-        !make_map(&mqc, L.q, s.d, s.N, (long long)s.B * s.H, QC, 1) ||
-        !make_map(&mgc, L.dout, s.d, s.N, (long long)s.B * s.H, QC, 1))
+        !make_map(&mqc, L.q, s.d, s.N, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1) ||
+        !make_map(&mgc, L.dout, s.d, s.N, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1))
         return cudaErrorNotSupported;
     DkvArgs a{L.alpha, L.lse, L.Dws, s, status, timeout_ns};
     const long long grid = (long long)s.B * s.Hkv * ((s.N + BK - 1) / BK);
