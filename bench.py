@@ -328,7 +328,8 @@ def reference_arm(args, w, rank, world):
 def config_block(w, l2_note):
     return {"workload": f"{w.name}: {w.description}", "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N,
             "d": w.d, "k_local": w.k_local, "period": w.period, "S": w.S,
-            "mode": "ecp" if w.mode == MODE_ECP else "pi", "input_dtype": w.dtype, "l2": l2_note}
+            "mode": {MODE_ECP: "ecp", MODE_PI_BIDIR: "pi_bidir"}.get(w.mode, "pi"),
+            "input_dtype": w.dtype, "l2": l2_note}
 
 
 def gpu_arm(args, w, rank, world, local_rank):
