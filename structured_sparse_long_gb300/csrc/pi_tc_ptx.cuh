@@ -52,18 +52,25 @@ struct WaitCtx {
 // Bounded wait on the phase of `bar` with the given parity.  Gives up when the
 // CTA's abort flag is raised, when another CTA has already recorded a failure in
 // the device status word (so a failing launch drains in one wave), or after
-// timeout_ns (then raises the flag and records the timeout).
+// timeout_ns (then raises the flag and records the timeout).  Those checks read
+// shared and global memory, and a phase that completes while such a read is in
+// flight goes unnoticed until it returns; so they run on every 32nd poll only, and
+// the timeout counts from the first of them.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx &w) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (n & 31u) continue;
         if (*w.abort) return false;
         if (w.status && *reinterpret_cast<volatile int *>(w.status) != kStatusOk) {
             *w.abort = 1u;
             return false;
         }
-        if (global_ns() - t0 > w.timeout_ns) {
+        const uint64_t now = global_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > w.timeout_ns) {
             *w.abort = 1u;
             record_status(w.status, kStatusTimeout);
             return false;
