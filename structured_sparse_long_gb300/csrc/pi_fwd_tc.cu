@@ -17,8 +17,9 @@
 //     chunks; each row attends to exactly one column of it (the "diagonal").
 //     Two chunks make one key tile (N <= 64).
 //   * Warp 0 (lane 0) streams Q and K tiles with TMA, warp 2 (lane 0) streams V
-//     tiles; warp 1 (lane 0) issues S = Q K^T into one of two 64-column TMEM
-//     buffers, warp 3 (lane 0) issues O += P V with P read from TMEM.
+//     tiles; warp 1 issues S = Q K^T into one of four 32-column TMEM buffers and
+//     warp 3 issues O += P V with P read from TMEM (each whole warp runs its loop,
+//     one elected lane issues the MMAs and commits).
 //   * Warps 4-7 run the softmax, one thread per row (TMEM lane = row): masks,
 //     adds the prior, keeps the running max m and sum l (rescaling O in TMEM
 //     only when the max grows by more than 2^8), writes P as bf16 over its S,
@@ -282,7 +283,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     auto timed_wait = [&](uint32_t b, uint32_t parity, int slot_base, int t) -> bool {
         const long long c0 = (DBG == 3) ? (long long)clock64() : 0;
         const bool r = wait_bar(b, parity, wc);
-        if (traced && t < kTraceTiles) args.trace[lin * kTraceSlots + slot_base + t] = (long long)clock64() - c0;
+        if (traced && t < kTraceTiles && lane == 0)
+            args.trace[lin * kTraceSlots + slot_base + t] = (long long)clock64() - c0;
         return r;
     };
     if (threadIdx.x == 0 && traced) {
@@ -423,66 +425,76 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
     } else if (warp == 1) {
         // ================= S issuer: S = Q K^T into the tile's TMEM buffer.  It runs ahead of
-        // the PV issuer, so that a PV never waits behind a K tile still in flight.
-        if (lane == 0) {
-            bool ok = wait_bar(bar(C::B_Q), 0, wc);
-            if (ok) stamp(3);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                const int st = t % KST, buf = t % NB;
-                if (!timed_wait(bar(C::B_KF + st), (t / KST) & 1, 104, t)) break;
-                // buffer buf last held P of tile t-NB: its PV must be done
-                if (t >= NB && !timed_wait(bar(C::B_PV + buf), ((t - NB) / NB) & 1, 120, t)) break;
-                tc_fence_after();
-                const int nch = min(CPT, n_chunks - CPT * t);
-                const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
-                const uint32_t dS = tbase + buf * TILE_N;
+        // the PV issuer, so that a PV never waits behind a K tile still in flight.  The whole warp
+        // runs the loop and its waits, so that descriptors and TMEM addresses are warp-uniform;
+        // one elected lane issues the MMAs and the commits.
+        bool ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_Q), 0, wc));
+        if (ok && lane == 0) stamp(3);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+            const int st = t % KST, buf = t % NB;
+            bool w = timed_wait(bar(C::B_KF + st), (t / KST) & 1, 104, t);
+            // buffer buf last held P of tile t-NB: its PV must be done
+            if (w && t >= NB) w = timed_wait(bar(C::B_PV + buf), ((t - NB) / NB) & 1, 120, t);
+            if (!__all_sync(0xffffffffu, w)) break;
+            tc_fence_after();
+            const int nch = min(CPT, n_chunks - CPT * t);
+            const uint32_t idesc = idesc_bf16(BM, CHUNK * nch, 0, 0);
+            const uint32_t dS = tbase + buf * TILE_N;
+            const uint64_t a0 = sdesc(sQ, 16, 1024);
+            const uint64_t b0 = sdesc(sK + st * C::KV_STAGE, 16, 1024);
+            if (elect_one()) {
 #pragma unroll
                 for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t a = sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024);
-                        const uint64_t bb =
-                            sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024);
+                        // the start address field counts 16-byte units
+                        const uint64_t a = a0 + (uint64_t)((dc * C::Q_DBLK + ks * 32) >> 4);
+                        const uint64_t bb = b0 + (uint64_t)((dc * C::KV_DBLK + ks * 32) >> 4);
                         mma_ss(dS, a, bb, idesc, (dc | ks) != 0);
                     }
                 }
-                stamp_tile(40, t);
                 tc_commit(bar(C::B_SF + buf));
                 tc_commit(bar(C::B_KE + st));
             }
-            // every MMA this thread issued has finished before TMEM is released
-            tc_commit(bar(C::B_DR));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR), 0, w2);
+            __syncwarp();
+            if (lane == 0) stamp_tile(40, t);
         }
+        // every MMA this warp issued has finished before TMEM is released
+        if (elect_one()) tc_commit(bar(C::B_DR));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR), 0, w2);
     } else if (warp == 3) {
-        // ================= PV issuer: O += P V with P read from TMEM
-        if (lane == 0) {
-            bool ok = true;
-            for (int u = 0; ok && u < n_tiles; ++u) {
-                const int st = u % VST, buf = u % NB;
-                if (!timed_wait(bar(C::B_PR + buf), (u / NB) & 1, 136, u)) break;
-                if (!timed_wait(bar(C::B_VF + st), (u / VST) & 1, 152, u)) break;
-                tc_fence_after();
-                const int nch = min(CPT, n_chunks - CPT * u);
-                const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
-                const uint32_t aP = tbase + buf * TILE_N;
-                for (int kk = 0; kk < 2 * nch; ++kk) {
-                    const uint64_t bb = sdesc(sV + st * C::KV_STAGE + kk * 16 * ROW_BYTES,
-                                              C::KV_DBLK, 1024);
-                    mma_ts(tbase + O_COL, aP + kk * 8, bb, idesc, (u > 0 || kk > 0) ? 1u : 0u);
-                }
-                stamp_tile(56, u);
+        // ================= PV issuer: O += P V with P read from TMEM (whole warp, one elected
+        // lane issuing, as for the S issuer)
+        bool ok = true;
+        for (int u = 0; ok && u < n_tiles; ++u) {
+            const int st = u % VST, buf = u % NB;
+            bool w = timed_wait(bar(C::B_PR + buf), (u / NB) & 1, 136, u);
+            if (w) w = timed_wait(bar(C::B_VF + st), (u / VST) & 1, 152, u);
+            if (!__all_sync(0xffffffffu, w)) break;
+            tc_fence_after();
+            const int nch = min(CPT, n_chunks - CPT * u);
+            const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
+            const uint32_t aP = tbase + buf * TILE_N;
+            const uint64_t b0 = sdesc(sV + st * C::KV_STAGE, C::KV_DBLK, 1024);
+            if (elect_one()) {
+                for (int kk = 0; kk < 2 * nch; ++kk)
+                    mma_ts(tbase + O_COL, aP + kk * 8, b0 + (uint64_t)((kk * 16 * ROW_BYTES) >> 4), idesc,
+                           (u > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar(C::B_PV + buf));
                 tc_commit(bar(C::B_VE + st));
                 if (u == n_tiles - 1) tc_commit(bar(C::B_OF));
             }
-            tc_commit(bar(C::B_DR2));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR2), 0, w2);
+            __syncwarp();
+            if (lane == 0) stamp_tile(56, u);
         }
+        if (elect_one()) tc_commit(bar(C::B_DR2));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR2), 0, w2);
     } else if (warp >= 4) {
         // ================= softmax + epilogue: one thread per row
         const int q4 = warp & 3;
