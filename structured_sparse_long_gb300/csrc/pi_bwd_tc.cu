@@ -254,52 +254,58 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
     } else if (warp == 1) {
         // ================= S/dP issuer: S = Q K^T and dP = dO V^T into buffer t & 1, as soon as
-        // that buffer's previous A1/A2 MMAs (tile t-2) are done
-        if (lane == 0) {
-            bool ok = wait_bar(bar(C::B_QF), 0, wc);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                const int st = t % ST, buf = t & 1;
-                if (!wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc)) break;
-                if (!wait_bar(bar(C::B_VF + st), (t / ST) & 1, wc)) break;
-                if (t >= 2 && !wait_bar(bar(C::B_BF + buf), ((t - 2) >> 1) & 1, wc)) break;
-                tc_fence_after();
-                const int nch = min(CPT, n_chunks - CPT * t);
-                const uint32_t idesc_s = idesc_bf16(BM, CHUNK * nch, 0, 0);
-                const uint32_t dS = tbase + C::S_COL + buf * C::BUF, dP = tbase + C::DP_COL + buf * C::BUF;
+        // that buffer's previous A1/A2 MMAs (tile t-2) are done.  The whole warp runs the loop and
+        // its waits (warp-uniform operands); one elected lane issues the MMAs and commits.
+        bool ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_QF), 0, wc));
+        const uint64_t q0 = sdesc(sQ, 16, 1024), g0 = sdesc(sG, 16, 1024);
+        for (int t = 0; ok && t < n_tiles; ++t) {
+            const int st = t % ST, buf = t & 1;
+            bool w = wait_bar(bar(C::B_KF + st), (t / ST) & 1, wc);
+            if (w) w = wait_bar(bar(C::B_VF + st), (t / ST) & 1, wc);
+            if (w && t >= 2) w = wait_bar(bar(C::B_BF + buf), ((t - 2) >> 1) & 1, wc);
+            if (!__all_sync(0xffffffffu, w)) break;
+            tc_fence_after();
+            const int nch = min(CPT, n_chunks - CPT * t);
+            const uint32_t idesc_s = idesc_bf16(BM, CHUNK * nch, 0, 0);
+            const uint32_t dS = tbase + C::S_COL + buf * C::BUF, dP = tbase + C::DP_COL + buf * C::BUF;
+            const uint64_t k0 = sdesc(sK + st * C::KV_STAGE, 16, 1024), v0 = sdesc(sV + st * C::KV_STAGE, 16, 1024);
+            if (elect_one()) {
 #pragma unroll
                 for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (dc | ks) != 0;
-                        mma_ss(dS, sdesc(sQ + dc * C::Q_DBLK + ks * 32, 16, 1024),
-                               sdesc(sK + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
-                               idesc_s, acc);
-                        mma_ss(dP, sdesc(sG + dc * C::Q_DBLK + ks * 32, 16, 1024),
-                               sdesc(sV + st * C::KV_STAGE + dc * C::KV_DBLK + ks * 32, 16, 1024),
-                               idesc_s, acc);
+                        // the start address field counts 16-byte units
+                        const uint64_t oq = (uint64_t)((dc * C::Q_DBLK + ks * 32) >> 4);
+                        const uint64_t okv = (uint64_t)((dc * C::KV_DBLK + ks * 32) >> 4);
+                        mma_ss(dS, q0 + oq, k0 + okv, idesc_s, acc);
+                        mma_ss(dP, g0 + oq, v0 + okv, idesc_s, acc);
                     }
                 }
                 tc_commit(bar(C::B_SF + buf));
                 tc_commit(bar(C::B_VE + st));  // V is read by dP only
             }
-            tc_commit(bar(C::B_DR));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR), 0, w2);
+            __syncwarp();
         }
+        if (elect_one()) tc_commit(bar(C::B_DR));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR), 0, w2);
     } else if (warp == 3) {
-        // ================= A1/A2 issuer: A1 += p (dp - c) K, A2 += p K from buffer t & 1
-        if (lane == 0) {
-            bool ok = true;
-            const uint32_t idesc_a = idesc_bf16(BM, D, 0, 1);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                const int st = t % ST, buf = t & 1;
-                // K of tile t landed before S of tile t, which the softmax saw before P
-                if (!wait_bar(bar(C::B_PR + buf), (t >> 1) & 1, wc)) break;
-                tc_fence_after();
-                const int nch = min(CPT, n_chunks - CPT * t);
+        // ================= A1/A2 issuer: A1 += p (dp - c) K, A2 += p K from buffer t & 1 (whole
+        // warp, one elected lane issuing)
+        const uint32_t idesc_a = idesc_bf16(BM, D, 0, 1);
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % ST, buf = t & 1;
+            // K of tile t landed before S of tile t, which the softmax saw before P
+            if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_PR + buf), (t >> 1) & 1, wc))) break;
+            tc_fence_after();
+            const int nch = min(CPT, n_chunks - CPT * t);
+            const uint64_t k0 = sdesc(sK + st * C::KV_STAGE, C::KV_DBLK, 1024);
+            if (elect_one()) {
                 for (int kk = 0; kk < 2 * nch; ++kk) {
-                    const uint64_t kb = sdesc(sK + st * C::KV_STAGE + kk * 16 * ROW_BYTES, C::KV_DBLK, 1024);
+                    const uint64_t kb = k0 + (uint64_t)((kk * 16 * ROW_BYTES) >> 4);
                     const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
                     mma_ts(tbase + C::A1_COL, tbase + C::S_COL + buf * C::BUF + kk * 8, kb, idesc_a, acc);
                     mma_ts(tbase + C::A2_COL, tbase + C::DP_COL + buf * C::BUF + kk * 8, kb, idesc_a, acc);
@@ -308,11 +314,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 tc_commit(bar(C::B_KE + st));  // K is read by S and by A1/A2, which come last
                 if (t == n_tiles - 1) tc_commit(bar(C::B_AF));
             }
-            tc_commit(bar(C::B_DR2));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR2), 0, w2);
+            __syncwarp();
         }
+        if (elect_one()) tc_commit(bar(C::B_DR2));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR2), 0, w2);
     } else if (warp >= 4) {
         // ================= one thread per query row
         const int q4 = warp & 3;
@@ -701,63 +709,70 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
     } else if (warp == 1) {
         // ================= S^T/dP^T issuer: into buffer ci & 1 once its previous dV/dK MMAs
-        // (chunk ci-2) are done
-        if (lane == 0) {
-            bool ok = wait_bar(bar(C::B_KV), 0, wc);
-            const uint32_t idesc_t = idesc_bf16(BK, QC, 0, 0);  // S^T, dP^T: both operands K-major
-            for (int ci = 0; ok && ci < n_chunks; ++ci) {
-                const int st = ci % ST, buf = ci & 1;
-                if (!wait_bar(bar(C::B_QF + st), (ci / ST) & 1, wc)) break;
-                if (ci >= 2 && !wait_bar(bar(C::B_BF + buf), ((ci - 2) >> 1) & 1, wc)) break;
-                tc_fence_after();
-                const uint32_t q_st = sQ + st * C::QC_BYTES, g_st = sG + st * C::QC_BYTES;
-                const uint32_t dS = tbase + C::ST_COL + buf * C::BUF, dP = tbase + C::DPT_COL + buf * C::BUF;
+        // (chunk ci-2) are done (whole warp, one elected lane issuing)
+        bool ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_KV), 0, wc));
+        const uint32_t idesc_t = idesc_bf16(BK, QC, 0, 0);  // S^T, dP^T: both operands K-major
+        const uint64_t kd0 = sdesc(sK, 16, 1024), vd0 = sdesc(sV, 16, 1024);
+        for (int ci = 0; ok && ci < n_chunks; ++ci) {
+            const int st = ci % ST, buf = ci & 1;
+            bool w = wait_bar(bar(C::B_QF + st), (ci / ST) & 1, wc);
+            if (w && ci >= 2) w = wait_bar(bar(C::B_BF + buf), ((ci - 2) >> 1) & 1, wc);
+            if (!__all_sync(0xffffffffu, w)) break;
+            tc_fence_after();
+            const uint64_t qd0 = sdesc(sQ + st * C::QC_BYTES, 16, 1024), gd0 = sdesc(sG + st * C::QC_BYTES, 16, 1024);
+            const uint32_t dS = tbase + C::ST_COL + buf * C::BUF, dP = tbase + C::DPT_COL + buf * C::BUF;
+            if (elect_one()) {
 #pragma unroll
                 for (int dc = 0; dc < C::KD; ++dc) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (dc | ks) != 0;
-                        mma_ss(dS, sdesc(sK + dc * C::KT_DBLK + ks * 32, 16, 1024),
-                               sdesc(q_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
-                        mma_ss(dP, sdesc(sV + dc * C::KT_DBLK + ks * 32, 16, 1024),
-                               sdesc(g_st + dc * C::QC_DBLK + ks * 32, 16, 1024), idesc_t, acc);
+                        // the start address field counts 16-byte units
+                        const uint64_t ok_ = (uint64_t)((dc * C::KT_DBLK + ks * 32) >> 4);
+                        const uint64_t oq = (uint64_t)((dc * C::QC_DBLK + ks * 32) >> 4);
+                        mma_ss(dS, kd0 + ok_, qd0 + oq, idesc_t, acc);
+                        mma_ss(dP, vd0 + ok_, gd0 + oq, idesc_t, acc);
                     }
                 }
                 tc_commit(bar(C::B_SF + buf));
             }
-            tc_commit(bar(C::B_DR));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR), 0, w2);
+            __syncwarp();
         }
+        if (elect_one()) tc_commit(bar(C::B_DR));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR), 0, w2);
     } else if (warp == 3) {
-        // ================= dV/dK issuer: dV += P^T dO, dK += dZ^T Q from buffer ci & 1
-        if (lane == 0) {
-            bool ok = true;
-            const uint32_t idesc_a = idesc_bf16(BK, D, 0, 1);   // dV, dK: B = chunk, MN-major
-            for (int ci = 0; ok && ci < n_chunks; ++ci) {
-                const int st = ci % ST, buf = ci & 1;
-                // the chunk's Q/dO landed before its S^T, which the key threads saw before P^T
-                if (!wait_bar(bar(C::B_PR + buf), (ci >> 1) & 1, wc)) break;
-                tc_fence_after();
-                const uint32_t q_st = sQ + st * C::QC_BYTES, g_st = sG + st * C::QC_BYTES;
+        // ================= dV/dK issuer: dV += P^T dO, dK += dZ^T Q from buffer ci & 1 (whole
+        // warp, one elected lane issuing)
+        const uint32_t idesc_a = idesc_bf16(BK, D, 0, 1);   // dV, dK: B = chunk, MN-major
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int st = ci % ST, buf = ci & 1;
+            // the chunk's Q/dO landed before its S^T, which the key threads saw before P^T
+            if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_PR + buf), (ci >> 1) & 1, wc))) break;
+            tc_fence_after();
+            const uint64_t qd0 = sdesc(sQ + st * C::QC_BYTES, C::QC_DBLK, 1024);
+            const uint64_t gd0 = sdesc(sG + st * C::QC_BYTES, C::QC_DBLK, 1024);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < QC / 16; ++kk) {
                     const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tbase + C::DV_COL, tbase + C::ST_COL + buf * C::BUF + kk * 8,
-                           sdesc(g_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
-                    mma_ts(tbase + C::DK_COL, tbase + C::DPT_COL + buf * C::BUF + kk * 8,
-                           sdesc(q_st + kk * 16 * ROW_BYTES, C::QC_DBLK, 1024), idesc_a, acc);
+                    const uint64_t o = (uint64_t)((kk * 16 * ROW_BYTES) >> 4);
+                    mma_ts(tbase + C::DV_COL, tbase + C::ST_COL + buf * C::BUF + kk * 8, gd0 + o, idesc_a, acc);
+                    mma_ts(tbase + C::DK_COL, tbase + C::DPT_COL + buf * C::BUF + kk * 8, qd0 + o, idesc_a, acc);
                 }
                 tc_commit(bar(C::B_BF + buf));
                 tc_commit(bar(C::B_QE + st));
                 if (ci == n_chunks - 1) tc_commit(bar(C::B_OF));
             }
-            tc_commit(bar(C::B_DR2));
-            volatile uint32_t zero = 0;
-            WaitCtx w2{&zero, args.status, args.timeout_ns};
-            wait_bar(bar(C::B_DR2), 0, w2);
+            __syncwarp();
         }
+        if (elect_one()) tc_commit(bar(C::B_DR2));
+        __syncwarp();
+        volatile uint32_t zero = 0;
+        WaitCtx w2{&zero, args.status, args.timeout_ns};
+        wait_bar(bar(C::B_DR2), 0, w2);
     } else if (warp >= 4) {
         // ================= one thread per key
         const int q4 = warp & 3;
