@@ -19,10 +19,10 @@
  *                                                           log-prior, one softmax
  *                                                           over the union)
  *   bidirectional pi mode (the same page, 2.1 and 2.2 in their general,
- *   non-causal form; forward only):
+ *   non-causal form; forward and backward):
  *     L(i) = { j : max(0, i - k_local) <= j <= min(N - 1, i + k_local) }
- *     P(i) = { i - m*period >= 0 and i + m*period < N : m = 1..S,
- *              m*period > k_local },   priors as in pi mode
+ *     P(i) = { i - m*period : i - m*period >= 0 } u { i + m*period : i + m*period < N },
+ *            m = 1..S with m*period > k_local,   priors as in pi mode
  *   ECP mode ("Efficient Context Propagating Perceiver Architectures for
  *   Auto-Regressive Language Modeling", section 2, paired-segment PAR block):
  *     with half-segment length c = k_local and s = floor(i / c):
@@ -56,8 +56,7 @@
  *                      ECP mode, where it is unused)
  *   PI_ERR_SHAPE       B, H, Hkv, N <= 0; H % Hkv != 0; k_local < 0; S < 0;
  *                      period <= 0 while S > 0; ECP with k_local <= 0 or S != 0
- *   PI_ERR_UNSUPPORTED d not in {32, 64, 128}; unknown mode; the backward in
- *                      bidirectional mode; sizes whose
+ *   PI_ERR_UNSUPPORTED d not in {32, 64, 128}; unknown mode; sizes whose
  *                      element offsets overflow int64 or whose row count
  *                      exceeds 2^31-1; (debug calls) N above their limit
  *   PI_ERR_ALIGN       a bf16/fp32 tensor of shape [.., d] not 16-byte aligned,

@@ -94,7 +94,6 @@ int run_bwd(const void *q, const void *k, const void *v, const float *alpha, con
     if (mode != PI_MODE_ECP && !alpha) return PI_ERR_NULL;
     const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     if (rc != PI_OK) return rc;
-    if (mode == PI_MODE_PI_BIDIR) return PI_ERR_UNSUPPORTED;  // the backward is causal/ECP only
     const void *p16[] = {q, k, v, out, dout, dq, dk, dv};
     for (const void *p : p16)
         if (!aligned(p, 16)) return PI_ERR_ALIGN;

@@ -55,9 +55,12 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
         : "memory");
 }
 
-// Key chunk walk of a q-block: identical enumeration to the forward kernel's.
+// Key chunk walk of a q-block: identical enumeration to the forward kernel's.  Skip blocks
+// follow the band: first the n_back blocks of keys i - m*period, then (bidirectional mode)
+// those of keys i + m*period, both for m = m_first, m_first + 1, ...; `back` is the distance
+// i - key of the chunk's keys (negative for keys after the query).
 struct QWalk {
-    int lo0, n_band, m_first, cpb, cpb_log2, p0, period;
+    int lo0, n_band, m_first, cpb, cpb_log2, p0, period, n_back;
     __device__ __forceinline__ int key0(int ci, int &back, bool &skip) const {
         if (ci < n_band) {
             back = 0;
@@ -65,9 +68,9 @@ struct QWalk {
             return lo0 + ci * CHUNK;
         }
         const int sc = ci - n_band;
-        const int m = m_first + (sc >> cpb_log2);
+        const int blk = sc >> cpb_log2;
         const int u = sc & (cpb - 1);
-        back = m * period;
+        back = (blk < n_back) ? (m_first + blk) * period : -(m_first + blk - n_back) * period;
         skip = true;
         return p0 - back + u * CHUNK;
     }
@@ -163,13 +166,19 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     cw.cpb = R / CHUNK;
     cw.cpb_log2 = (cw.cpb == 4) ? 2 : (cw.cpb == 2) ? 1 : 0;
     cw.lo0 = band_lo(p0, s.mode, s.k_local);
-    cw.n_band = (min(s.N - 1, p0 + R - 1) - cw.lo0) / CHUNK + 1;
+    cw.n_band = (band_hi(min(s.N - 1, p0 + R - 1), s.N, s.mode, s.k_local) - cw.lo0) / CHUNK + 1;
     int n_skip_blocks = 0;
     cw.m_first = 1;
-    if (s.mode == 0 && s.S > 0) {
+    cw.n_back = 0;
+    if (s.mode != kModeEcp && s.S > 0) {
         cw.m_first = max(1, s.k_local / s.period + 1);
-        const int m_last = min(s.S, (p0 + R - 1) / s.period);
-        n_skip_blocks = max(0, m_last - cw.m_first + 1);
+        const int m_last = min(s.S, (p0 + R - 1) / s.period);  // some row has i - m*period >= 0
+        cw.n_back = max(0, m_last - cw.m_first + 1);
+        n_skip_blocks = cw.n_back;
+        if (s.mode == kModeBidir) {
+            const int m_last_f = min(s.S, (s.N - 1 - p0) / s.period);  // some row has i + m*period < N
+            n_skip_blocks += max(0, m_last_f - cw.m_first + 1);
+        }
     }
     const int n_chunks = cw.n_band + n_skip_blocks * cw.cpb;
     constexpr int CPT = C::CPT;
@@ -331,11 +340,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const bool row_ok = i < s.N;
         const long long row_g = ((long long)b * s.H + h) * s.N + i;
         const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
-        const float off_band = (s.mode == 0) ? log2f(al) : 0.f;
+        const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
         const float off_skip = log2f(1.f - al);
         const float lse2 = row_ok ? args.lse[row_g] * kLog2e : -INFINITY;
         const bool live = row_ok && lse2 != -INFINITY;
         const int lo_i = band_lo(i, s.mode, s.k_local);
+        const int hi_i = band_hi(i, s.N, s.mode, s.k_local);
         const float sc = s.scale_log2;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         float dsum = 0.f, skip_p = 0.f, skip_pdp = 0.f;
@@ -377,11 +387,11 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 float off;
                 if (!sk) {
                     clo = max(lo_i - key0, 0);
-                    chi = min(i - key0, CHUNK - 1);
+                    chi = min(hi_i - key0, CHUNK - 1);
                     off = off_band;
                 } else {
                     const int jk = i - back, c = jk - key0;
-                    if (jk >= 0 && c >= 0 && c < CHUNK) { clo = c; chi = c; }
+                    if (jk >= 0 && jk < s.N && c >= 0 && c < CHUNK) { clo = c; chi = c; }
                     else { clo = CHUNK; chi = -1; }
                     off = off_skip;
                     any_skip |= (clo <= chi);
@@ -468,7 +478,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (args.dalpha) {
                 any_skip = any_skip && live;
                 args.dalpha[row_g] =
-                    (s.mode == 0 && any_skip) ? -(skip_pdp - dsum * skip_p) / (al * (1.f - al)) : 0.f;
+                    (s.mode != kModeEcp && any_skip) ? -(skip_pdp - dsum * skip_p) / (al * (1.f - al)) : 0.f;
             }
         }
     }
@@ -506,21 +516,24 @@ static cudaError_t launch_dq(const CUtensorMap &mq, const CUtensorMap &mg, const
 constexpr int BK = 128;     // keys per CTA (M)
 
 // The query chunks (qc queries each) that attend to keys [j0, j0 + 128) of one KV head, for
-// one query head: band chunks i0 = j0 + qc*c up to the last query whose band holds key
-// j0 + 127, then 128/qc chunks per skip multiple m (queries j0 + m*period + [0, 128)).
+// one query head: band chunks i0 = q0 + qc*c from the first query whose band holds key j0 to
+// the last whose band holds key j0 + 127; then 128/qc chunks per skip multiple m: first the
+// n_fwd multiples of queries j0 + m*period + [0, 128) (their keys i - m*period), then
+// (bidirectional mode) those of queries j0 - m*period + [0, 128) (keys i + m*period).  `back` is
+// the distance query - key of a skip chunk.
 struct KWalk {
-    int j0, n_band, m_first, n_skip, period, per_head, qc, cps_log2;
+    int j0, q0, n_band, m_first, n_fwd, n_skip, period, per_head, qc, cps_log2;
     __device__ __forceinline__ void chunk(int ci, int &hh, int &i0, int &back, bool &skip) const {
         hh = ci / per_head;
         const int c = ci - hh * per_head;
         if (c < n_band) {
-            i0 = j0 + c * qc;
+            i0 = q0 + c * qc;
             back = 0;
             skip = false;
         } else {
             const int sc = c - n_band;
-            const int m = m_first + (sc >> cps_log2);
-            back = m * period;
+            const int blk = sc >> cps_log2;
+            back = (blk < n_fwd) ? (m_first + blk) * period : -(m_first + blk - n_fwd) * period;
             i0 = j0 + back + (sc & ((1 << cps_log2) - 1)) * qc;
             skip = true;
         }
@@ -609,14 +622,22 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     kw.qc = QC;
     kw.cps_log2 = C::CPS_LOG2;
     const int qlast = band_last_query(min(s.N - 1, kw.j0 + BK - 1), s.N, s.mode, s.k_local);
-    kw.n_band = (qlast - kw.j0) / QC + 1;
+    kw.q0 = band_first_query(kw.j0, s.mode, s.k_local);
+    kw.n_band = (qlast - kw.q0) / QC + 1;
     kw.m_first = 1;
+    kw.n_fwd = 0;
     kw.n_skip = 0;
-    if (s.mode == 0 && s.S > 0) {
+    if (s.mode != kModeEcp && s.S > 0) {
         kw.m_first = max(1, s.k_local / s.period + 1);
-        // multiples whose first skip query is inside the sequence
+        // multiples whose first skip query j0 + m*period is inside the sequence
         const int m_last = min(s.S, (s.N - 1 - kw.j0) / s.period);
-        kw.n_skip = (1 << C::CPS_LOG2) * max(0, m_last - kw.m_first + 1);
+        kw.n_fwd = max(0, m_last - kw.m_first + 1);
+        int n_blocks = kw.n_fwd;
+        if (s.mode == kModeBidir) {  // multiples whose last skip query j0 + 127 - m*period is >= 0
+            const int m_last_b = min(s.S, min(s.N - 1, kw.j0 + BK - 1) / s.period);
+            n_blocks += max(0, m_last_b - kw.m_first + 1);
+        }
+        kw.n_skip = (1 << C::CPS_LOG2) * n_blocks;
     }
     kw.per_head = kw.n_band + kw.n_skip;
     const int n_chunks = G * kw.per_head;
@@ -695,10 +716,10 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             for (int e = 0; e < QC / 32; ++e) {
                 const int c = lane + 32 * e, i = i0 + c;
                 float bias = -INFINITY, dv = 0.f;
-                if (i < s.N) {
+                if (i >= 0 && i < s.N) {  // skip chunks of the bidirectional mode may start before 0
                     const float lse2 = args.lse[rbase + i] * kLog2e;
                     const float al = args.alpha ? args.alpha[rbase + i] : 1.f;
-                    const float prior = (s.mode != 0) ? 0.f : (sk ? log2f(1.f - al) : log2f(al));
+                    const float prior = (s.mode == kModeEcp) ? 0.f : (sk ? log2f(1.f - al) : log2f(al));
                     if (lse2 != -INFINITY) bias = prior - lse2;
                     dv = args.Dws[rbase + i];
                 }
@@ -780,6 +801,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const int j = kw.j0 + r;
         const bool key_ok = j < s.N;
         const int qlast_j = key_ok ? band_last_query(j, s.N, s.mode, s.k_local) : -1;
+        const int qfirst_j = band_first_query(j, s.mode, s.k_local);
         const float sc = s.scale_log2;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         bool ok = true;
@@ -799,11 +821,11 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             // valid query columns of this key: [clo, chi]
             int clo, chi;
             if (!sk) {
-                clo = max(j - i0, 0);
+                clo = max(qfirst_j - i0, 0);
                 chi = min(qlast_j - i0, QC - 1);
             } else {
-                const int c = j + back - i0;
-                if (j + back < s.N && c >= 0 && c < QC) { clo = c; chi = c; }
+                const int iq = j + back, c = iq - i0;
+                if (iq >= 0 && iq < s.N && c >= 0 && c < QC) { clo = c; chi = c; }
                 else { clo = QC; chi = -1; }
             }
             if (!key_ok) { clo = QC; chi = -1; }

@@ -56,6 +56,13 @@ __host__ __device__ __forceinline__ int band_hi(int i, int N, int mode, int k_lo
     return hi > N - 1 ? N - 1 : (int)hi;
 }
 
+// First query position whose band contains key j (for key-major passes): the band of i reaches
+// back to i - k, or (ECP) to the previous half-segment's start, which is never after j for i >= j.
+__host__ __device__ __forceinline__ int band_first_query(int j, int mode, int k_local) {
+    if (mode != kModeBidir) return j;
+    return j - k_local < 0 ? 0 : j - k_local;
+}
+
 // Last query position whose band contains key j (for key-major passes).
 __host__ __device__ __forceinline__ int band_last_query(int j, int N, int mode, int k_local) {
     long long hi;

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
     }
     __syncwarp();
     const float al = a.alpha ? a.alpha[row] : 1.f;
-    const float off_b = (s.mode == 0) ? log2f(al) : 0.f;
+    const float off_b = (s.mode != kModeEcp) ? log2f(al) : 0.f;
     const float off_s = log2f(1.f - al);
     const float lse2 = a.lse[row] * kLog2e;
     constexpr int RC = D / 32;
@@ -232,19 +232,21 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
         }
     };
 
-    const int lo = band_lo(i, s.mode, s.k_local);
-    for (int j0 = lo; j0 <= i; j0 += 32) {
+    const int lo = band_lo(i, s.mode, s.k_local), hi = band_hi(i, s.N, s.mode, s.k_local);
+    for (int j0 = lo; j0 <= hi; j0 += 32) {
         const int j = j0 + lane;
-        chunk(j, j <= i, off_b, false);
+        chunk(j, j <= hi, off_b, false);
     }
-    if (s.mode == 0) {
-        for (int m0 = 1; m0 <= s.S; m0 += 32) {
-            const int mm = m0 + lane;
-            const long long back = (long long)mm * s.period;
-            const long long jj = (long long)i - back;
-            const bool valid = mm <= s.S && back > s.k_local && jj >= 0;
-            any_skip |= valid;
-            chunk(valid ? (int)jj : 0, valid, off_s, true);
+    if (s.mode != kModeEcp) {
+        for (int dir = -1; dir <= ((s.mode == kModeBidir) ? 1 : -1); dir += 2) {  // i - m pi, i + m pi
+            for (int m0 = 1; m0 <= s.S; m0 += 32) {
+                const int mm = m0 + lane;
+                const long long back = (long long)mm * s.period;
+                const long long jj = (long long)i + dir * back;
+                const bool valid = mm <= s.S && back > s.k_local && jj >= 0 && jj < s.N;
+                any_skip |= valid;
+                chunk(valid ? (int)jj : 0, valid, off_s, true);
+            }
         }
     }
     const float Drow = warp_sum(d_part);
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
     if (lane == 0) {
         a.Dws[row] = Drow;
         if (a.dalpha)
-            a.dalpha[row] = (s.mode == 0 && any_skip) ? -sdz / (al * (1.f - al)) : 0.f;
+            a.dalpha[row] = (s.mode != kModeEcp && any_skip) ? -sdz / (al * (1.f - al)) : 0.f;
     }
 }
 
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
                 const float lse2 = a.lse[row] * kLog2e;
                 if (lse2 != -INFINITY) {
                     const float al = a.alpha ? a.alpha[row] : 1.f;
-                    const float off = (s.mode == 0) ? (is_skip ? log2f(1.f - al) : log2f(al)) : 0.f;
+                    const float off = (s.mode != kModeEcp) ? (is_skip ? log2f(1.f - al) : log2f(al)) : 0.f;
                     const float z = fmaf(dot_row<T, D>(ks[warp], qb + (long long)i * D), s.scale_log2, off);
                     p = exp2f(z - lse2);
                     const float dp = dot_row<T, D>(vs[warp], gb + (long long)i * D);
@@ -323,18 +325,22 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
             }
         };
 
+        const int ifirst = band_first_query(j, s.mode, s.k_local);
         const int ilast = band_last_query(j, s.N, s.mode, s.k_local);
-        for (int i0 = j; i0 <= ilast; i0 += 32) {
+        for (int i0 = ifirst; i0 <= ilast; i0 += 32) {
             const int i = i0 + lane;
             chunk(i, i <= ilast, false);
         }
-        if (s.mode == 0) {
-            for (int m0 = 1; m0 <= s.S; m0 += 32) {
-                const int mm = m0 + lane;
-                const long long back = (long long)mm * s.period;
-                const long long ii = (long long)j + back;
-                const bool valid = mm <= s.S && back > s.k_local && ii < s.N;
-                chunk(valid ? (int)ii : 0, valid, true);
+        if (s.mode != kModeEcp) {
+            // queries j + m pi (whose skip key i - m pi is j) and, bidirectionally, j - m pi
+            for (int dir = 1; dir >= ((s.mode == kModeBidir) ? -1 : 1); dir -= 2) {
+                for (int m0 = 1; m0 <= s.S; m0 += 32) {
+                    const int mm = m0 + lane;
+                    const long long back = (long long)mm * s.period;
+                    const long long ii = (long long)j + dir * back;
+                    const bool valid = mm <= s.S && back > s.k_local && ii >= 0 && ii < s.N;
+                    chunk(valid ? (int)ii : 0, valid, true);
+                }
             }
         }
     }

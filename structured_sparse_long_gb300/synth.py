@@ -14,6 +14,8 @@ Context Propagating Perceiver Architectures...", section 2, PAR block):
   C5  training fwd+bwd bf16       B2 H16 Hkv16 N16384 d64  k256 pi512  S2
   C6  bidirectional GQA bf16 fwd  B1 H16 Hkv4  N65536 d128 k256 pi1024 S4 (band i-k..i+k,
                                   skips i -/+ m*pi: the general form of the same page, 2.1-2.2)
+  C7  bidirectional training bf16 B2 H16 Hkv16 N16384 d64  k256 pi512  S2, fwd+bwd (C5's
+                                  shapes in the bidirectional form)
   D4  decode step, C4 layer       B64 H16 Hkv4 cache N16384 d128 k256 pi1024 S4: one new
                                   query per sequence (q [B,H,d], alpha [B,H]) against the cache
 
@@ -80,6 +82,9 @@ WORKLOADS = {
     "C6": Workload("C6", 1, 16, 4, 65536, 128, 256, 1024, 4, MODE_PI_BIDIR, "bf16", 5, "unit",
                    "sigmoid(1.5)",
                    description="long-context GQA bf16 bidirectional pi-Attention fwd"),
+    "C7": Workload("C7", 2, 16, 16, 16384, 64, 256, 512, 2, MODE_PI_BIDIR, "bf16", 7, "unit",
+                   "sigmoid(1.0)", backward=True,
+                   description="training fwd+bwd bf16 bidirectional pi-Attention"),
     "D4": Workload("D4", 64, 16, 4, 16384, 128, 256, 1024, 4, MODE_PI, "bf16", 6, "unit",
                    "sigmoid(1.5)", decode=True,
                    description="decode step of the long-context GQA layer, 64 sequences"),

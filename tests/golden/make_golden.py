@@ -1,6 +1,6 @@
 """Writes tests/golden/pair_counts.json using only the oracle (oracle.counts).
 
-The per-(b, h) attended-pair totals and key-index sums of the six workloads.
+The per-(b, h) attended-pair totals and key-index sums of the seven workloads.
 Neighbour sets: "pi-Attention: Periodic Sparse Transformers for Efficient
 Long-Context Modeling" section 2.1 (causal band [i-k, i]) and 2.2 (skip keys
 i - m*pi, m = 1..S, kept when m*pi > k and i - m*pi >= 0); ECP page section 2
@@ -25,6 +25,7 @@ WORKLOADS = {
     "C4": dict(N=65536, k_local=256, period=1024, S=4, mode=0),
     "C5": dict(N=16384, k_local=256, period=512, S=2, mode=0),
     "C6": dict(N=65536, k_local=256, period=1024, S=4, mode=2),
+    "C7": dict(N=16384, k_local=256, period=512, S=2, mode=2),
 }
 
 

@@ -106,7 +106,9 @@ def test_bwd_validation(lib, fn):
     assert bwd_call(lib, dalpha=A16 + 1, fn=fn) == PI_ERR_ALIGN
     assert bwd_call(lib, ws=None, fn=fn) == PI_ERR_WORKSPACE
     assert bwd_call(lib, ws_bytes=16, fn=fn) == PI_ERR_WORKSPACE
-    assert bwd_call(lib, mode=2, fn=fn) == PI_ERR_UNSUPPORTED  # the backward is causal/ECP only
+    assert bwd_call(lib, mode=2, alpha=None, fn=fn) == PI_ERR_NULL   # bidirectional needs alpha
+    assert bwd_call(lib, mode=2, ws=None, fn=fn) == PI_ERR_WORKSPACE  # validated like pi mode
+    assert bwd_call(lib, mode=3, fn=fn) == PI_ERR_UNSUPPORTED
 
 
 def dec_call(lib, q=A16, kc=A16, vc=A16, alpha=A16, B=1, H=4, Hkv=2, N=64, d=64, kl=8, per=16, S=1,

@@ -295,7 +295,7 @@ def test_counts_closed_forms(case):
 
 
 def test_golden_pair_counts():
-    """Per-(b,h) attended-pair totals of the five workloads (tests/golden/pair_counts.json)."""
+    """Per-(b,h) attended-pair totals of the workloads (tests/golden/pair_counts.json)."""
     with open(os.path.join(GOLDEN, "pair_counts.json")) as f:
         gold = json.load(f)
     for name, rec in gold["workloads"].items():
