@@ -4,7 +4,8 @@
 
 A step is one pass of the hot path over one batch of synthetic input: the
 fused forward (band tiles + skip gather + GQA + epilogue) for the forward
-workloads, forward + backward for the training workload C5.  The default
+workloads, forward + backward for the training workloads C5 (causal) and C7
+(bidirectional).  The default
 workload is C4 (B1 H16 Hkv4 N65536 d128 k256 pi1024 S4, bf16), the N=65536
 configuration the roofline target is stated for.
 
