@@ -37,12 +37,17 @@ namespace tc {
 
 constexpr int BM = 128;           // rows per CTA (MMA M)
 constexpr int CHUNK = 32;         // keys per chunk (TMA box rows)
-#ifndef PI_FWD_CPT
-#define PI_FWD_CPT 1
-#endif
-constexpr int CPT = PI_FWD_CPT;   // chunks per key tile (1 or 2)
-constexpr int TILE_N = CPT * CHUNK;
-constexpr int NB = 4 / CPT;       // S buffers: NB x TILE_N = 128 TMEM columns
+// Chunks per key tile (the N of the S products is 32 * CPT) and S buffers, NB x TILE_N = 128
+// TMEM columns.  At d = 128 the S products of 32-key tiles cost the pipe its per-instruction
+// minimum, but four buffers keep S of tile t+4 from waiting on more than PV of tile t; at d = 64
+// the eight S products of a 64-key tile take no longer than those of a 32-key tile, and two
+// buffers suffice.
+template <int D>
+struct Tiling {
+    static constexpr int CPT = (D == 64) ? 2 : 1;
+    static constexpr int TILE_N = CPT * CHUNK;
+    static constexpr int NB = 4 / CPT;
+};
 constexpr int NUM_THREADS = 256;
 constexpr int TMEM_COLS = 256;    // S buffers [0,128), O [128, 128+d)
 constexpr int O_COL = 128;
@@ -52,6 +57,7 @@ constexpr float kRescaleThreshold = 8.f;      // log2 units
 
 template <int D>
 struct Cfg {
+    static constexpr int CPT = Tiling<D>::CPT, TILE_N = Tiling<D>::TILE_N, NB = Tiling<D>::NB;
     static constexpr int KD = D / 64;  // 64-element column blocks of d
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_STAGE = TILE_N * D * 2;
@@ -254,6 +260,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const TcArgs args) {
     using C = Cfg<D>;
     constexpr int KST = C::KSTAGES, VST = C::VSTAGES;
+    constexpr int CPT = C::CPT, TILE_N = C::TILE_N, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
