@@ -310,6 +310,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int g = h0 / (s.H / s.Hkv);
     const int p0 = pb * R;
 
+    // ---- Q first: its load is the longest wait of the block's set-up
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmQ);
+        mbar_init(bar(C::B_Q), 1u);
+        fence_barrier_init();
+        mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
+        for (int dc = 0; dc < C::KD; ++dc)
+            tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
+                             policy_evict_first());
+        stamp(2);
+    }
+
     // ---- key chunks of this block
     ChunkWalk cw;
     cw.p0 = p0;
@@ -348,7 +360,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // arrivals), TMEM
     if (warp == 0) {
         for (int idx = lane; idx < C::NBARS; idx += 32)
-            mbar_init(bar(idx), (idx >= C::B_PR && idx < C::B_PR + NB) ? 128u : 1u);
+            if (idx != C::B_Q) mbar_init(bar(idx), (idx >= C::B_PR && idx < C::B_PR + NB) ? 128u : 1u);
         if (lane == 0) *abort_flag = 0u;
         fence_barrier_init();
         __syncwarp();
@@ -367,16 +379,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                                  key0, b * s.Hkv + g, bar(full_bar + st), policy);
         }
     };
-    // Q and the first K tile, which the first S = Q K^T waits for, go out before the CTA
-    // barrier, so that their latency overlaps the TMEM allocation and the barrier itself.
+    // The first K tile, which the first S = Q K^T waits for, goes out before the CTA barrier, so
+    // that its latency overlaps the TMEM allocation and the barrier itself.
     if (threadIdx.x == 0) {
-        prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
-        mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
-        for (int dc = 0; dc < C::KD; ++dc)
-            tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_Q),
-                             policy_evict_first());
-        stamp(2);
         stamp_tile(8, 0);
         issue_kv(&tmK, sK, C::B_KF, KST, 0, policy_evict_last());
     }
