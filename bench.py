@@ -116,11 +116,36 @@ KERNEL_SOURCES = {
 PROFILE_NAMES = {"fwd": "pi_fwd_tc", "bwd": "pi_bwd_tc", "dec": "pi_decode"}
 
 
+def _code_only(src: str) -> str:
+    """C++/CUDA source without comments and with whitespace runs collapsed: what the compiler sees."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":  # string or character literal, copied as is
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha(kind: str = "fwd") -> str:
+    """Hash of the kernel's sources as compiled: comments and layout do not change it."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "structured_sparse_long_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "structured_sparse_long_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -15,11 +15,12 @@
 //     band chunk (keys lo(p0) + 32c ...) or a skip chunk: the keys i - m*period
 //     of the block's rows form R consecutive keys, so one skip block is R/32
 //     chunks; each row attends to exactly one column of it (the "diagonal").
-//     Two chunks make one key tile (N <= 64).
+//     A key tile is one chunk at d = 128 and two at d = 64 (Tiling<D>).
 //   * Warp 0 (lane 0) streams Q and K tiles with TMA, warp 2 (lane 0) streams V
-//     tiles; warp 1 issues S = Q K^T into one of four 32-column TMEM buffers and
-//     warp 3 issues O += P V with P read from TMEM (each whole warp runs its loop,
-//     one elected lane issues the MMAs and commits).
+//     tiles; warp 1 issues S = Q K^T into one of the 128 columns of TMEM S
+//     buffers (four of 32 or two of 64) and warp 3 issues O += P V with P read
+//     from TMEM (each whole warp runs its loop, one elected lane issues the MMAs
+//     and commits).
 //   * Warps 4-7 run the softmax, one thread per row (TMEM lane = row): masks,
 //     adds the prior, keeps the running max m and sum l (rescaling O in TMEM
 //     only when the max grows by more than 2^8), writes P as bf16 over its S,
