@@ -61,6 +61,8 @@ def _load():
         lib.oracle_fwd.restype = I
         lib.oracle_bwd.argtypes = [P, P, P, I, P, P, L, L, L, L, L, L, L, I, I, P, P, P, P]
         lib.oracle_bwd.restype = I
+        lib.oracle_gate.argtypes = [P, I, P, P, L, L, L, L, P]
+        lib.oracle_gate.restype = None
         _lib = lib
         return lib
 
@@ -162,6 +164,41 @@ def bwd(q, k, v, alpha, dout, k_local, period, S, mode):
     if rc != 0:
         raise ValueError("oracle_bwd: bad arguments")
     return dq, dk, dv, dal
+
+
+def gate(q, w, c):
+    """Gate alpha [B,H,N] (float64): 1 / (1 + exp(-(q . w_h + c_h))) for every query row.
+
+    q [B,H,N,d] (bf16, fp32 or fp64), w [H,d] and c [H] (any float type; taken as fp64).
+    The pi-Attention page, 2.3, names a light per-token, per-head network producing alpha
+    from the input content; this is its one-layer reading on the head's query.
+    """
+    lib = _load()
+    qa, dt = _as_raw(q)
+    B, H, N, d = qa.shape
+    wa = np.ascontiguousarray(_np64(w).reshape(H, d))
+    ca = np.ascontiguousarray(_np64(c).reshape(H))
+    alpha = np.zeros((B, H, N), dtype=np.float64)
+    lib.oracle_gate(_ptr(qa), dt, _ptr(wa), _ptr(ca), B, H, N, d, _ptr(alpha))
+    return alpha
+
+
+def fwd_gated(q, k, v, w, c, k_local, period, S, mode, rows=None):
+    """Forward with alpha from the gate (rounded to fp32, the precision the forward takes alpha
+    in).  Returns (out, lse, alpha) with alpha the fp64 gate."""
+    alpha = gate(q, w, c)
+    out, lse = fwd(q, k, v, alpha.astype(np.float32), k_local, period, S, mode, rows=rows)
+    return out, lse, alpha
+
+
+def _np64(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().cpu().double().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
 
 
 def threads() -> int:

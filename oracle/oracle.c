@@ -41,6 +41,11 @@
  *   dv_j = sum_{h in group, i} p_ij dout_i
  *   dalpha_i = sum_{j local} dz_ij / alpha_i - sum_{j skip} dz_ij / (1 - alpha_i)
  *
+ * Gate (same page, 2.3: a light per-token, per-head network producing alpha
+ * from the input content).  Reading: a one-layer logistic gate on the head's
+ * query, alpha_{b,h,i} = 1 / (1 + exp(-(q_{b,h,i} . w_h + c_h))), w [H, d],
+ * c [H]; the query projection is the network's first layer.
+ *
  * Inputs may be fp64, fp32 or raw bf16 bits; bf16 is widened exactly.  All
  * arithmetic is fp64.  Parallel over query rows with OpenMP.
  */
@@ -298,4 +303,19 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
     }
     free(qd); free(kd); free(vd); free(gd);
     return 0;
+}
+
+/*
+ * Gate: alpha [B, H, N] fp64 from q [B, H, N, d] (any input dtype), w [H, d] and c [H]
+ * (fp64).  alpha = 1 / (1 + exp(-(q . w_h + c_h))).
+ */
+void oracle_gate(const void *q, int dt, const double *w, const double *c, long B, long H, long N,
+                 long d, double *alpha) {
+#pragma omp parallel for schedule(static)
+    for (long row = 0; row < B * H * N; ++row) {
+        const long h = (row / N) % H;
+        double z = c[h];
+        for (long t = 0; t < d; ++t) z += ld(q, dt, (size_t)row * d + t) * w[h * d + t];
+        alpha[row] = 1.0 / (1.0 + exp(-z));
+    }
 }
