@@ -114,6 +114,25 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
                     int mode, void *out, float *lse, void *stream);
 
 /*
+ * pi_attn_fwd_gated -- pi_attn_fwd with the gate fused into the same launch
+ * ("pi-Attention" page, section 2.3: a light per-token, per-head network produces
+ * alpha from the input content).  Reading of the network: a one-layer logistic
+ * gate on the head's query,
+ *     alpha_{b,h,i} = 1 / (1 + exp(-(q_{b,h,i} . gate_w[h] + gate_b[h]))),
+ * computed in fp32 from the bf16 query row the kernel has already staged, then
+ * used exactly as pi_attn_fwd uses its alpha input.
+ *   gate_w [H, d] fp32 (16-byte aligned), gate_b [H] fp32, alpha_out [B, H, N] fp32
+ *   (may be NULL; receives the gate's alpha, e.g. for pi_attn_bwd, whose dalpha is then
+ *   the gradient with respect to these values).  mode: pi or bidirectional (ECP:
+ *   PI_ERR_UNSUPPORTED); d: 64 or 128 (else PI_ERR_UNSUPPORTED).  Other arguments,
+ *   layouts and errors as pi_attn_fwd.
+ */
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w,
+                      const float *gate_b, int B, int H, int Hkv, int N, int d, int k_local,
+                      int period, int S, int mode, void *out, float *lse, float *alpha_out,
+                      void *stream);
+
+/*
  * pi_attn_bwd_workspace_size -- bytes of device workspace pi_attn_bwd needs
  * for these sizes: one fp32 per query row for D_i = sum_j p_ij (dout_i . v_j),
  * which equals dout_i . out_i in exact arithmetic; it is recomputed from the

@@ -8,10 +8,10 @@ the first call loads the library and fails loudly if it is missing.
 """
 from ._binding import (MODE_ECP, MODE_PI, MODE_PI_BIDIR, PiAttnError, bwd, bwd_noalloc,  # noqa: F401
                        bwd_workspace_size, decode,
-                       debug_counts, debug_probs, debug_trace, debug_wait_timeout, fwd, lib_path,
+                       debug_counts, debug_probs, debug_trace, debug_wait_timeout, fwd, fwd_gated, lib_path,
                        load,
                        status, strerror)
 
-__all__ = ["fwd", "bwd", "decode", "bwd_noalloc", "bwd_workspace_size", "status", "strerror", "debug_counts",
+__all__ = ["fwd", "fwd_gated", "bwd", "decode", "bwd_noalloc", "bwd_workspace_size", "status", "strerror", "debug_counts",
            "debug_probs", "debug_trace", "debug_wait_timeout", "load", "lib_path", "PiAttnError",
            "MODE_PI", "MODE_ECP", "MODE_PI_BIDIR"]

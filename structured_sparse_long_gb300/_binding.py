@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
         lib.pi_attn_debug_trace.restype = I
         lib.pi_attn_decode.argtypes = [P, P, P, P] + [I] * 9 + [P, P, P]
         lib.pi_attn_decode.restype = I
+        lib.pi_attn_fwd_gated.argtypes = [P, P, P, P, P] + [I] * 9 + [P, P, P, P]
+        lib.pi_attn_fwd_gated.restype = I
         for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
                      "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
                      "pi_attn_debug_wait_timeout"):
@@ -138,6 +140,34 @@ def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
             _ptr(out), _ptr(lse), _stream(stream))
     _check(fn.__name__, rc)
     return out, lse
+
+
+def fwd_gated(q, k, v, gate_w, gate_b, k_local: int, period: int, S: int, mode: int = MODE_PI,
+              out=None, lse=None, alpha_out=None, stream=None):
+    """pi_attn_fwd_gated (bf16, d 64 or 128): the forward with the gate
+    alpha = 1 / (1 + exp(-(q . gate_w[h] + gate_b[h]))) computed in the same launch.
+    gate_w [H, d] and gate_b [H] fp32.  Returns (out, lse, alpha)."""
+    B, H, Hkv, N, d = _sizes(q, k)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _expect(t, n, torch.bfloat16)
+    _expect(v, "v", torch.bfloat16, k.shape)
+    _expect(gate_w, "gate_w", torch.float32, (H, d))
+    _expect(gate_b, "gate_b", torch.float32, (H,))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if alpha_out is None:
+        alpha_out = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _expect(out, "out", torch.bfloat16, q.shape)
+    _expect(lse, "lse", torch.float32, (B, H, N))
+    _expect(alpha_out, "alpha_out", torch.float32, (B, H, N))
+    lib = load()
+    rc = lib.pi_attn_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_w), _ptr(gate_b), B, H, Hkv, N, d,
+                               k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(alpha_out),
+                               _stream(stream))
+    _check("pi_attn_fwd_gated", rc)
+    return out, lse, alpha_out
 
 
 def decode(q, k_cache, v_cache, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,

@@ -160,6 +160,29 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
                    0, nullptr, nullptr, nullptr, nullptr);
 }
 
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w,
+                      const float *gate_b, int B, int H, int Hkv, int N, int d, int k_local, int period,
+                      int S, int mode, void *out, float *lse, float *alpha_out, void *stream) {
+    if (!gate_w || !gate_b) return PI_ERR_NULL;
+    // the gate is the pi mode's (causal or bidirectional); ECP has no prior to weight
+    if (mode != PI_MODE_PI && mode != PI_MODE_PI_BIDIR) return PI_ERR_UNSUPPORTED;
+    const int rc = validate_fwd(q, k, v, gate_b, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
+    if (rc != PI_OK) return rc;
+    if (d != 64 && d != 128) return PI_ERR_UNSUPPORTED;  // the tensor-core forward only
+    if (!aligned(gate_w, 16) || !aligned(gate_b, 4) || (alpha_out && !aligned(alpha_out, 4))) return PI_ERR_ALIGN;
+    int *status = status_word();
+    if (!status) return PI_ERR_CUDA;
+    pi::LaunchFwd L;
+    L.q = q; L.k = k; L.v = v; L.alpha = nullptr;
+    L.out = out; L.lse = lse;
+    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    L.fp32 = false; L.dbg = 0; L.cnt = nullptr; L.isum = nullptr; L.lse_in = nullptr; L.P = nullptr;
+    L.trace = nullptr; L.n_trace = 0;
+    L.status = status; L.timeout_ns = kWaitTimeoutNs;
+    L.gate_w = gate_w; L.gate_b = gate_b; L.alpha_out = alpha_out;
+    return map_cuda(pi::launch_fwd_tc(L, static_cast<cudaStream_t>(stream)));
+}
+
 size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
     (void)Hkv;
     (void)d;

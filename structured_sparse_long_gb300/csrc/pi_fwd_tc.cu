@@ -218,6 +218,9 @@ struct TcArgs {
     float *P;
     long long *trace;  // DBG 3: clock64() stamps, kTraceSlots per traced CTA
     int n_trace;       // DBG 3: CTAs 0 .. n_trace-1 are traced
+    const float *gate_w;  // fused gate (or null): alpha = 1 / (1 + exp(-(q_i . gate_w[h] + gate_b[h])))
+    const float *gate_b;
+    float *alpha_out;     // [B, H, N] the gate's alpha (may be null)
 };
 
 // Trace layout (DBG 3), slots per CTA: 0 entry, 1 set-up done, 2 Q issued, 3 Q landed (MMA
@@ -518,7 +521,36 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int h = h0 + hh;
         const bool row_ok = i < s.N;
         const long long row_g = ((long long)b * s.H + h) * s.N + i;
-        const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
+        float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
+        if (args.gate_w) {
+            // Fused gate ("pi-Attention" page, 2.3): a per-token, per-head logistic gate on this
+            // row of the Q tile, alpha = 1 / (1 + exp(-(q_i . w_h + c_h))).  The rows past N
+            // read the zero fill and are not written.
+            if (__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), 0, wc))) {
+                const float *wh = args.gate_w + (size_t)h * D;
+                float z0 = args.gate_b[h], z1 = 0.f;
+#pragma unroll
+                for (int dc = 0; dc < C::KD; ++dc) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {  // 8 bf16 of the row per 16-byte chunk
+                        const uint4 u = *reinterpret_cast<const uint4 *>(smem + C::Q_OFF + dc * C::Q_DBLK +
+                                                                         r * ROW_BYTES + ((ch ^ (r & 7)) << 4));
+                        const float4 wa = *reinterpret_cast<const float4 *>(wh + dc * 64 + ch * 8);
+                        const float4 wb = *reinterpret_cast<const float4 *>(wh + dc * 64 + ch * 8 + 4);
+                        z0 = fmaf(__uint_as_float(u.x << 16), wa.x, z0);
+                        z1 = fmaf(__uint_as_float(u.x & 0xffff0000u), wa.y, z1);
+                        z0 = fmaf(__uint_as_float(u.y << 16), wa.z, z0);
+                        z1 = fmaf(__uint_as_float(u.y & 0xffff0000u), wa.w, z1);
+                        z0 = fmaf(__uint_as_float(u.z << 16), wb.x, z0);
+                        z1 = fmaf(__uint_as_float(u.z & 0xffff0000u), wb.y, z1);
+                        z0 = fmaf(__uint_as_float(u.w << 16), wb.z, z0);
+                        z1 = fmaf(__uint_as_float(u.w & 0xffff0000u), wb.w, z1);
+                    }
+                }
+                al = 1.f / (1.f + __expf(-(z0 + z1)));
+                if (args.alpha_out && row_ok) args.alpha_out[row_g] = al;
+            }
+        }
         const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
         const float off_skip = log2f(1.f - al);
         const int lo_i = band_lo(i, s.mode, s.k_local);
@@ -787,7 +819,7 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     int m_first = 1;
     if (s.mode != kModeEcp && s.S > 0) m_first = s.k_local / s.period + 1;  // smallest m with m*period > k
     TcArgs a{L.alpha, L.lse, s, GP, m_first, L.status, L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P,
-             L.trace, L.n_trace};
+             L.trace, L.n_trace, L.gate_w, L.gate_b, L.alpha_out};
     if (s.H / GP > 65535 || s.B > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)((s.N + R - 1) / R), (unsigned)(s.H / GP), (unsigned)s.B);
     if (s.d == 64) {

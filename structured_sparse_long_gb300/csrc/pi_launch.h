@@ -24,6 +24,11 @@ struct LaunchFwd {
     int n_trace;           // dbg 3: number of traced CTAs
     int *status;           // device status word
     uint64_t timeout_ns;   // bound on every device-side wait
+    // fused gate (tensor-core path): alpha = 1 / (1 + exp(-(q_i . gate_w[h] + gate_b[h]))) is
+    // computed in the kernel instead of read from alpha; alpha_out (may be null) receives it
+    const float *gate_w = nullptr;  // [H, d]
+    const float *gate_b = nullptr;  // [H]
+    float *alpha_out = nullptr;     // [B, H, N]
 };
 
 struct LaunchBwd {

@@ -154,3 +154,12 @@ def small_case(name="case", B=1, H=2, Hkv=2, N=300, d=64, k_local=40, period=64,
     """A parity-test workload of arbitrary (small) shape."""
     return Workload(name, B, H, Hkv, N, d, k_local, period, S, mode, dtype, seed, qkv_scale,
                     alpha, backward)
+
+
+def gate_weights(H: int, d: int, seed: int):
+    """Synthetic weights of the fused gate: w [H, d] ~ N(0, 1/d) and c [H] ~ N(0, 1), fp32, so that
+    for unit-variance queries the gate logit q . w_h + c_h has about unit spread."""
+    gen = torch.Generator().manual_seed(seed)
+    w = torch.randn(H, d, generator=gen, dtype=torch.float32) / math.sqrt(d)
+    c = torch.randn(H, generator=gen, dtype=torch.float32)
+    return w, c

@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     for n in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
               "pi_attn_bwd_workspace_size", "pi_attn_status", "pi_attn_strerror",
               "pi_attn_debug_counts", "pi_attn_debug_probs", "pi_attn_debug_wait_timeout",
-              "pi_attn_decode", "pi_attn_bwd_noalloc", "pi_attn_debug_trace"):
+              "pi_attn_decode", "pi_attn_bwd_noalloc", "pi_attn_debug_trace", "pi_attn_fwd_gated"):
         assert n in names
 
 
@@ -89,6 +89,26 @@ def test_fwd_validation(lib, fn):
     assert fwd_call(lib, v=A16 + 2, fn=fn) == PI_ERR_ALIGN
     assert fwd_call(lib, out=A16 + 4, fn=fn) == PI_ERR_ALIGN
     assert fwd_call(lib, lse=A16 + 2, fn=fn) == PI_ERR_ALIGN
+
+
+def gated_call(lib, q=A16, gw=A16, gb=A16, B=1, H=2, Hkv=2, N=64, d=64, kl=8, per=16, S=1, mode=0,
+               out=A16, lse=A16, aout=A16):
+    return lib.pi_attn_fwd_gated(q, A16, A16, gw, gb, B, H, Hkv, N, d, kl, per, S, mode, out, lse, aout,
+                                 None)
+
+
+def test_fwd_gated_validation(lib):
+    assert gated_call(lib, gw=None) == PI_ERR_NULL
+    assert gated_call(lib, gb=None) == PI_ERR_NULL
+    assert gated_call(lib, q=None) == PI_ERR_NULL
+    assert gated_call(lib, mode=1, kl=16, S=0) == PI_ERR_UNSUPPORTED   # ECP has no gate
+    assert gated_call(lib, mode=3) == PI_ERR_UNSUPPORTED
+    assert gated_call(lib, d=32) == PI_ERR_UNSUPPORTED                 # tensor-core path only
+    assert gated_call(lib, H=3, Hkv=2) == PI_ERR_SHAPE
+    assert gated_call(lib, gw=A16 + 4) == PI_ERR_ALIGN                 # float4 loads of w
+    assert gated_call(lib, gb=A16 + 2) == PI_ERR_ALIGN
+    assert gated_call(lib, aout=A16 + 2) == PI_ERR_ALIGN
+    assert gated_call(lib, q=A16 + 8) == PI_ERR_ALIGN
 
 
 def bwd_call(lib, ws=A16, ws_bytes=1 << 20, dq=A16, alpha=A16, d=64, dalpha=A16, N=64, mode=0,
