@@ -37,7 +37,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from structured_sparse_long_gb300.synth import MODE_ECP, MODE_PI_BIDIR, WORKLOADS, make_inputs  # noqa: E402
+from structured_sparse_long_gb300.synth import (MODE_ECP, MODE_PI_BIDIR, WORKLOADS, gate_weights,  # noqa: E402
+                                                make_inputs)
 
 METRIC = "sparse-attn tokens/s and useful TFLOP/s at N=4K–64K; % of roofline (1×GB300)"
 L2_BYTES = 129 * 1024 * 1024
@@ -245,8 +246,13 @@ class OracleSample:
     def run(self, npos: int) -> float:
         w = self.w
         t0 = time.perf_counter()
-        self.oracle.fwd(self.inp["q"], self.inp["k"], self.inp["v"], self.inp["alpha"], w.k_local,
-                        w.period, w.S, w.mode, rows=(w.N - npos, w.N))
+        if w.gate:
+            gw, gb = gate_weights(w.H, w.d, w.seed + 100)
+            self.oracle.fwd_gated(self.inp["q"], self.inp["k"], self.inp["v"], gw, gb, w.k_local,
+                                  w.period, w.S, w.mode, rows=(w.N - npos, w.N))
+        else:
+            self.oracle.fwd(self.inp["q"], self.inp["k"], self.inp["v"], self.inp["alpha"], w.k_local,
+                            w.period, w.S, w.mode, rows=(w.N - npos, w.N))
         return time.perf_counter() - t0
 
     def size_for(self, target_s: float) -> int:
@@ -383,9 +389,17 @@ def gpu_arm(args, w, rank, world, local_rank):
                     ws=torch.empty(max(16, pa.bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)),
                                    device=dev, dtype=torch.uint8))
 
+    if w.gate:  # the gate's weights are parameters, resident like the model's
+        gw, gb = (t.to(dev) for t in gate_weights(w.H, w.d, w.seed + 100))
+        alpha_buf = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+
     def fwd():
-        pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
-               lse=lse, stream=stream)
+        if w.gate:
+            pa.fwd_gated(d["q"], d["k"], d["v"], gw, gb, w.k_local, w.period, w.S, w.mode, out=out,
+                         lse=lse, alpha_out=alpha_buf, stream=stream)
+        else:
+            pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
+                   lse=lse, stream=stream)
 
     def bwd():
         pa.bwd(d["q"], d["k"], d["v"], d["alpha"], out, lse, d["dout"], w.k_local, w.period, w.S,

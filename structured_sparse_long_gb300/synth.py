@@ -16,6 +16,8 @@ Context Propagating Perceiver Architectures...", section 2, PAR block):
                                   skips i -/+ m*pi: the general form of the same page, 2.1-2.2)
   C7  bidirectional training bf16 B2 H16 Hkv16 N16384 d64  k256 pi512  S2, fwd+bwd (C5's
                                   shapes in the bidirectional form)
+  C8  gated long-context GQA     C4's layer with the fused gate: alpha = sigmoid(q . w_h + c_h)
+                                  computed in the forward launch (gate_weights(H, d, seed + 100))
   D4  decode step, C4 layer       B64 H16 Hkv4 cache N16384 d128 k256 pi1024 S4: one new
                                   query per sequence (q [B,H,d], alpha [B,H]) against the cache
 
@@ -55,6 +57,7 @@ class Workload:
     backward: bool = False
     description: str = ""
     decode: bool = False  # one new query per (b, h) against a KV cache of N rows (row N-1)
+    gate: bool = False    # alpha from the fused gate (weights: gate_weights(H, d, seed + 100))
 
     @property
     def tokens(self) -> int:
@@ -85,6 +88,8 @@ WORKLOADS = {
     "C7": Workload("C7", 2, 16, 16, 16384, 64, 256, 512, 2, MODE_PI_BIDIR, "bf16", 7, "unit",
                    "sigmoid(1.0)", backward=True,
                    description="training fwd+bwd bf16 bidirectional pi-Attention"),
+    "C8": Workload("C8", 1, 16, 4, 65536, 128, 256, 1024, 4, MODE_PI, "bf16", 8, "unit", "none",
+                   gate=True, description="long-context GQA bf16 pi-Attention fwd with the fused gate"),
     "D4": Workload("D4", 64, 16, 4, 16384, 128, 256, 1024, 4, MODE_PI, "bf16", 6, "unit",
                    "sigmoid(1.5)", decode=True,
                    description="decode step of the long-context GQA layer, 64 sequences"),
