@@ -55,3 +55,30 @@ def test_work_accounting_matches_closed_forms():
     assert wk["pairs"] == 17061760 * 16
     assert wk["fwd_bytes"] == 2 * 268435456 + 2 * 67108864 + 2 * 4 * 16 * 65536
     assert bench.pairs_per_head(8192, 512, 0, 0, 1) == 6033408
+
+
+def test_work_accounting_of_the_bidirectional_and_gated_workloads():
+    """C7 counts the bidirectional pairs (the golden per-head total, from the oracle), forward
+    and backward bytes; C8 moves the bytes of C4 (its alpha is written by the gate instead of
+    read)."""
+    import json
+    import os
+    import bench
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pair_counts.json")))
+    w7 = bench.WORKLOADS["C7"]
+    wk7 = bench.work(w7, True)
+    assert wk7["pairs"] == gold["workloads"]["C7"]["pairs_per_head"] * w7.B * w7.H
+    qo = w7.B * w7.H * w7.N * w7.d * 2
+    kv = w7.B * w7.Hkv * w7.N * w7.d * 2
+    vec = w7.B * w7.H * w7.N * 4
+    assert wk7["bwd_bytes"] == 4 * qo + 4 * kv + 3 * vec
+    assert wk7["bwd_flops"] == 8 * w7.d * wk7["pairs"]
+    assert bench.work(bench.WORKLOADS["C8"], False) == bench.work(bench.WORKLOADS["C4"], False)
+
+
+def test_gated_oracle_sample_runs_on_host_cores():
+    """The CPU-baseline leg of the gated workload drives the oracle's gate and forward."""
+    import bench
+    w = bench.WORKLOADS["C8"].replace(N=512)
+    smp = bench.OracleSample(w)
+    assert smp.run(16) > 0.0
