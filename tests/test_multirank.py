@@ -82,3 +82,25 @@ def test_gated_oracle_sample_runs_on_host_cores():
     w = bench.WORKLOADS["C8"].replace(N=512)
     smp = bench.OracleSample(w)
     assert smp.run(16) > 0.0
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """Rank 0 of the reference arm (the oracle on host cores) prints one JSON line with the
+    contract's keys, its own cpu_baseline and an e2e with no host-device bytes."""
+    import json
+    import bench
+
+    class A:
+        warmup, steps, gpus = 3, 1, 1
+    bench.reference_arm(A, bench.WORKLOADS["C1"], rank=0, world=1)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "impl",
+                "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["value"] > 0 and rec["unit"] == "tokens/s"
+    assert rec["config"]["workload"].startswith("C1")
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
