@@ -104,3 +104,15 @@ def test_reference_arm_prints_one_contract_line(capsys):
     assert rec["config"]["workload"].startswith("C1")
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_and_layout():
+    """Captures stay matched to code, not to comments: the hash's source text drops comments and
+    collapses whitespace but keeps string literals (PTX) intact."""
+    import bench
+    a = 'int x = 1;  // note\n/* block\n comment */ asm("mov.u32 %0, 1; // not a comment");\n'
+    b = 'int x = 1;\n\n asm("mov.u32 %0, 1; // not a comment");'
+    c = 'int x = 2;\n asm("mov.u32 %0, 1; // not a comment");'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert "// not a comment" in bench._code_only(a)
