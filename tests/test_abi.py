@@ -169,3 +169,9 @@ def test_binding_fails_loudly_without_cuda():
     q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
     with pytest.raises((ValueError, RuntimeError)):
         pa.fwd(q, q, q, torch.ones(1, 2, 8), 4, 8, 1)
+    with pytest.raises((ValueError, RuntimeError)):
+        pa.fwd_gated(q, q, q, torch.zeros(2, 64), torch.zeros(2), 4, 8, 1)
+    with pytest.raises((ValueError, RuntimeError)):
+        pa.decode(q[:, :, 0].contiguous(), q, q, torch.ones(1, 2), 4, 8, 1)
+    with pytest.raises((ValueError, RuntimeError)):
+        pa.bwd(q, q, q, torch.ones(1, 2, 8), q, torch.zeros(1, 2, 8), q, 4, 8, 1)
