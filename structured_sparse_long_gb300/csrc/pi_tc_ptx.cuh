@@ -55,27 +55,33 @@ struct WaitCtx {
 // timeout_ns (then raises the flag and records the timeout).  Those checks read
 // shared and global memory, and a phase that completes while such a read is in
 // flight goes unnoticed until it returns; so they run on every 32nd poll only, and
-// the timeout counts from the first of them.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx &w) {
-    if (mbar_try_wait(bar, parity)) return true;
+// the timeout counts from the first of them.  The first test is inlined at each wait;
+// the polling loop has one out-of-line copy, which keeps the kernels' hot loops small
+// (their instruction fetch is a measured limiter).
+static __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
+                                                  int *status, uint64_t timeout_ns) {
     uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if (n & 31u) continue;
-        if (*w.abort) return false;
-        if (w.status && *reinterpret_cast<volatile int *>(w.status) != kStatusOk) {
-            *w.abort = 1u;
+        if (*abort) return false;
+        if (status && *reinterpret_cast<volatile int *>(status) != kStatusOk) {
+            *abort = 1u;
             return false;
         }
         const uint64_t now = global_ns();
         if (t0 == 0) {
             t0 = now;
-        } else if (now - t0 > w.timeout_ns) {
-            *w.abort = 1u;
-            record_status(w.status, kStatusTimeout);
+        } else if (now - t0 > timeout_ns) {
+            *abort = 1u;
+            record_status(status, kStatusTimeout);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx &w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, w.abort, w.status, w.timeout_ns);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
