@@ -192,6 +192,27 @@ __device__ __forceinline__ float tile_raw_max(const uint32_t *r) {
 
 // ------------------------------------------------------------------ kernel
 
+// Division by a divisor fixed for the launch, as a multiply and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994: with
+// l = ceil(log2 d) and m = floor(2^(32+l) / d) + 1, floor(n / d) = floor(n m / 2^(32+l)) for
+// every 32-bit n).  The dividends here are below 2^31, so n * m (m < 2^33) fits 64 bits.
+struct FastDiv {
+    uint64_t m;
+    int sh;
+    __device__ __forceinline__ int div(int n) const {
+        return (int)(((unsigned long long)(unsigned)n * m) >> sh);
+    }
+};
+static inline FastDiv make_fastdiv(int d) {
+    int l = 0;
+    while ((1LL << l) < (long long)d) ++l;
+    const unsigned __int128 num = (unsigned __int128)1 << (32 + l);
+    FastDiv f;
+    f.m = (uint64_t)(num / (unsigned)d) + 1;
+    f.sh = 32 + l;
+    return f;
+}
+
 struct TcArgs {
     const float *alpha;
     float *lse;
@@ -200,6 +221,9 @@ struct TcArgs {
     int m_first;  // smallest skip multiple m with m * period > k_local (at most S + 1)
     int nqb;      // position blocks per (batch entry, head group)
     int ngrp;     // head groups (H / GP)
+    int R;        // positions per block, 128 / GP
+    int cpb_log2; // log2 of the tiles per skip block (R / 32)
+    FastDiv div_nqb, div_ngrp, div_G, div_period;  // by nqb, ngrp, H / Hkv, period
     int n_blocks; // blocks in all: nqb * ngrp * B; CTA c processes blocks c, c + gridDim.x, ...
     int *status;
     uint64_t timeout_ns;
@@ -258,19 +282,19 @@ struct BlockDesc {
 // Block L (positions fastest, then head groups, then batch entries) and its key tiles.
 __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc &d) {
     const Shape &s = a.s;
-    const int R = BM / a.GP;
-    const int rest = L / a.nqb;
+    const int R = a.R;
+    const int rest = a.div_nqb.div(L);
     const int pb = L - rest * a.nqb;
-    const int b = rest / a.ngrp;
+    const int b = a.div_ngrp.div(rest);
     d.h0 = (rest - b * a.ngrp) * a.GP;
     d.b = b;
-    d.g = d.h0 / (s.H / s.Hkv);
+    d.g = a.div_G.div(d.h0);
     d.p0 = pb * R;
     ChunkWalk &cw = d.cw;
     cw.p0 = d.p0;
     cw.period = s.period;
-    cw.cpb = R / CHUNK;
-    cw.cpb_log2 = (cw.cpb == 4) ? 2 : (cw.cpb == 2) ? 1 : 0;
+    cw.cpb_log2 = a.cpb_log2;
+    cw.cpb = 1 << a.cpb_log2;
     cw.lo0 = band_lo(d.p0, s.mode, s.k_local);
     const int blk_hi = band_hi(min(s.N - 1, d.p0 + R - 1), s.N, s.mode, s.k_local);
     cw.n_band = (blk_hi - cw.lo0) / CHUNK + 1;
@@ -278,11 +302,11 @@ __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc
     cw.m_first = a.m_first;
     cw.n_back = 0;
     if (s.mode != kModeEcp && s.S > 0) {
-        const int m_last = min(s.S, (d.p0 + R - 1) / s.period);  // some row has i - m*period >= 0
+        const int m_last = min(s.S, a.div_period.div(d.p0 + R - 1));  // some row has i - m*period >= 0
         cw.n_back = max(0, m_last - cw.m_first + 1);
         n_skip_blocks = cw.n_back;
         if (s.mode == kModeBidir) {
-            const int m_last_f = min(s.S, (s.N - 1 - d.p0) / s.period);  // some row has i + m*period < N
+            const int m_last_f = min(s.S, a.div_period.div(s.N - 1 - d.p0));  // some row has i + m*period < N
             n_skip_blocks += max(0, m_last_f - cw.m_first + 1);
         }
     }
@@ -633,8 +657,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ================= softmax + epilogue: one thread per row
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
-        const int R = BM / args.GP;
-        const int hh = r / R, trow = r % R;
+        const int R = args.R;
+        const int hh = r >> (5 + args.cpb_log2), trow = r & (R - 1);  // R = 32 << cpb_log2
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const float sc = s.scale_log2;
 
@@ -942,8 +966,10 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     const long long nb64 = (long long)nqb * ngrp * s.B;
     if (nb64 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int n_blocks = (int)nb64;
-    TcArgs a{L.alpha, L.lse, s, GP, m_first, nqb, ngrp, n_blocks, L.status, L.timeout_ns, L.cnt, L.isum,
-             L.lse_in, L.P, L.trace, L.n_trace, L.gate_w, L.gate_b, L.alpha_out};
+    const int cpb_log2 = (R == 128) ? 2 : (R == 64) ? 1 : 0;
+    TcArgs a{L.alpha, L.lse, s, GP, m_first, nqb, ngrp, R, cpb_log2, make_fastdiv(nqb), make_fastdiv(ngrp),
+             make_fastdiv(G), make_fastdiv(s.S > 0 && s.period > 0 ? s.period : 1), n_blocks, L.status,
+             L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P, L.trace, L.n_trace, L.gate_w, L.gate_b, L.alpha_out};
     // The forward runs persistent, two CTAs per SM; the debug modes take one CTA per block.
     unsigned grid = (unsigned)n_blocks;
     if (L.dbg == 0) {
