@@ -663,12 +663,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const float sc = s.scale_log2;
 
         // This row of block bd's Q tile into TMEM (rows past N hold the TMA's zero fill).
-        // Returns the row's alpha: the input's, or the fused gate's 1 / (1 + exp(-logit)).
+        // Returns the row's alpha: the input's, or the fused gate's 1 / (1 + exp(-logit)).  The
+        // input's is loaded after the out-of-line copy (a load in flight across a call would
+        // be waited for there); it was prefetched into L2 a block ahead.
         auto copy_q = [&](const BlockDesc &bd, int kb, float &al_out) -> bool {
             const int i = bd.p0 + trow, h = bd.h0 + hh;
             const bool row_ok = i < s.N;
             const long long row_g = ((long long)bd.b * s.H + h) * s.N + i;
-            al_out = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;  // issued before the wait
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), (uint32_t)(kb & 1), wc))) return false;
             const float *wh = args.gate_w ? args.gate_w + (size_t)h * D : nullptr;
             const float z = copy_q_row<D>(smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL, wh,
@@ -679,6 +680,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (wh) {
                 al_out = 1.f / (1.f + __expf(-z));
                 if (args.alpha_out && row_ok) args.alpha_out[row_g] = al_out;
+            } else {
+                al_out = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
             }
             return true;
         };
@@ -704,6 +707,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
             float m_ref = -INFINITY, l = 0.f;
             long long cnt = 0, isum = 0;
+            if (has_next && args.alpha) {  // the next block's alpha into L2, a block ahead
+                const int Ln = L + LS;     // < n_blocks
+                const int rest = args.div_nqb.div(Ln);
+                const int bn = args.div_ngrp.div(rest);
+                const int in = (Ln - rest * args.nqb) * R + trow;
+                if (in < s.N)
+                    prefetch_l2(args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.N + in);
+            }
 
             for (int t = 0; t < bd.n_tiles; ++t, ++gsm) {
                 const int buf = (int)(gsm % NB);
