@@ -247,8 +247,8 @@ class OracleSample:
         w = self.w
         t0 = time.perf_counter()
         if w.gate:
-            gw, gb = gate_weights(w.H, w.d, w.seed + 100)
-            self.oracle.fwd_gated(self.inp["q"], self.inp["k"], self.inp["v"], gw, gb, w.k_local,
+            gate = gate_weights(w.H, w.d, w.seed + 100)
+            self.oracle.fwd_gated(self.inp["q"], self.inp["k"], self.inp["v"], gate, w.k_local,
                                   w.period, w.S, w.mode, rows=(w.N - npos, w.N))
         else:
             self.oracle.fwd(self.inp["q"], self.inp["k"], self.inp["v"], self.inp["alpha"], w.k_local,
@@ -364,109 +364,9 @@ def config_block(w, l2_note):
             "input_dtype": w.dtype, "l2": l2_note}
 
 
-def gpu_arm(args, w, rank, world, local_rank):
-    import structured_sparse_long_gb300 as pa
-    from structured_sparse_long_gb300 import build as pbuild
-
-    if rank == 0 or not os.path.exists(pbuild.LIB_PATH):
-        pbuild.build()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    pa.load()
-    stream = torch.cuda.current_stream(dev)
-
-    inp = make_inputs(w, with_dout=w.backward)
-    d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
-    out = torch.empty_like(d["q"])
-    lse = torch.empty((w.B, w.H) if w.decode else (w.B, w.H, w.N), device=dev, dtype=torch.float32)
-    bufs = {}
-    if w.backward:
-        bufs = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]),
-                    dv=torch.empty_like(d["v"]),
-                    dalpha=torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32),
-                    ws=torch.empty(max(16, pa.bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)),
-                                   device=dev, dtype=torch.uint8))
-
-    if w.gate:  # the gate's weights are parameters, resident like the model's
-        gw, gb = (t.to(dev) for t in gate_weights(w.H, w.d, w.seed + 100))
-        alpha_buf = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
-
-    def fwd():
-        if w.gate:
-            pa.fwd_gated(d["q"], d["k"], d["v"], gw, gb, w.k_local, w.period, w.S, w.mode, out=out,
-                         lse=lse, alpha_out=alpha_buf, stream=stream)
-        else:
-            pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
-                   lse=lse, stream=stream)
-
-    def bwd():
-        pa.bwd(d["q"], d["k"], d["v"], d["alpha"], out, lse, d["dout"], w.k_local, w.period, w.S,
-               w.mode, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], dalpha=bufs["dalpha"],
-               workspace=bufs["ws"], stream=stream)
-
-    def dec():
-        pa.decode(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
-                  lse=lse, stream=stream)
-
-    # (name, launcher, kernels it launches)
-    if w.decode:
-        phases = [("pi_attn_decode", dec, 1)]
-    else:
-        phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 3)] if w.backward else [])
-    wk = work(w, w.backward)
-    flush = wk["bytes"] < 2 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, device=dev, dtype=torch.float32) if flush else None
-    l2_note = ("L2 flushed between steps (write of a 2x L2 buffer outside the timed events)"
-               if flush else f"inputs larger than L2 ({wk['bytes'] / 1e6:.0f} MB moved per step)")
-
-    def step(record=None):
-        for name, fn, _ in phases:
-            if record is not None:
-                record[name][0].record(stream)
-            fn()
-            if record is not None:
-                record[name][1].record(stream)
-
-    for _ in range(args.warmup):
-        if flush:
-            scratch.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    if pa.status() != 0:
-        raise RuntimeError("device status word set during warm-up")
-
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for n, _, _ in phases} for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    for k in range(args.steps):
-        if flush:
-            scratch.zero_()
-        step(ev[k])
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
-    status = pa.status()
-    if status != 0:
-        raise RuntimeError(f"device status word {status} after the timed region")
-
-    per_phase = {n: [e[n][0].elapsed_time(e[n][1]) for e in ev] for n, _, _ in phases}
-    step_ms = [sum(per_phase[n][k] for n, _, _ in phases) for k in range(args.steps)]
-    total_ms = sum(step_ms)
-    total_ms = reduce_max(total_ms, world, dev if args.backend == "nccl" else "cpu")
-    ms_per_step = total_ms / args.steps
-    tokens_per_step = (w.B if w.decode else w.B * w.N) * world
-    value = tokens_per_step * args.steps / (total_ms / 1e3)
-    tflops = wk["flops"] * world * args.steps / (total_ms / 1e3) / 1e12
-
-    # dominant kernel roofline (forward kernel: the whole step for the forward workloads)
+def roofline_of(w, wk, per_phase):
+    """Roofline of the step's dominant kernel: its algorithmic bytes (or useful FLOPs) per launch
+    over its mean launch time, against the measured peak that bounds it."""
     peaks, peak_kind = load_peaks()
     dom = max(per_phase, key=lambda n: sum(per_phase[n]))
     dom_ms = statistics.mean(per_phase[dom])
@@ -483,13 +383,170 @@ def gpu_arm(args, w, rank, world, local_rank):
         achieved, peak, unit = dom_flops / (dom_ms / 1e3) / 1e12, tensor, "TFLOP/s"
     traffic = profiled_traffic(w.name, {"pi_attn_fwd": "fwd", "pi_attn_bwd": "bwd",
                                         "pi_attn_decode": "dec"}[dom])
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
-                "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}, burst)",
-                "t_roof_us": 1e6 * max(t_hbm, t_tensor), "t_hbm_us": 1e6 * t_hbm,
-                "t_tensor_us": 1e6 * t_tensor, "kernel_us": 1e3 * dom_ms,
-                "algorithmic_bytes": dom_bytes, "useful_flops": dom_flops,
-                "tensor_frac_of_peak": dom_flops / (dom_ms / 1e3) / 1e12 / tensor}
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+            "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'}, burst)",
+            "t_roof_us": 1e6 * max(t_hbm, t_tensor), "t_hbm_us": 1e6 * t_hbm,
+            "t_tensor_us": 1e6 * t_tensor, "kernel_us": 1e3 * dom_ms,
+            "algorithmic_bytes": dom_bytes, "useful_flops": dom_flops,
+            "tensor_frac_of_peak": dom_flops / (dom_ms / 1e3) / 1e12 / tensor}
+
+
+def setup_workload(w, pa, dev, stream):
+    """Device inputs and outputs of a workload and the launchers of its step: returns (inputs on
+    the host, device tensors, out, lse, gradient buffers, phases), each phase (name, launcher,
+    kernels it launches)."""
+    inp = make_inputs(w, with_dout=w.backward)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.H) if w.decode else (w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    bufs = {}
+    if w.backward:
+        bufs = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]),
+                    dv=torch.empty_like(d["v"]),
+                    dalpha=torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32),
+                    ws=torch.empty(max(16, pa.bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)),
+                                   device=dev, dtype=torch.uint8))
+    gate = alpha_buf = None
+    if w.gate:  # the gate's weights are parameters, resident like the model's
+        gate = tuple(t.to(dev) for t in gate_weights(w.H, w.d, w.seed + 100))
+        alpha_buf = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+
+    def fwd():
+        if w.gate:
+            pa.fwd_gated(d["q"], d["k"], d["v"], gate, w.k_local, w.period, w.S, w.mode, out=out,
+                         lse=lse, alpha_out=alpha_buf, stream=stream)
+        else:
+            pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
+                   lse=lse, stream=stream)
+
+    def bwd():
+        pa.bwd(d["q"], d["k"], d["v"], d["alpha"], out, lse, d["dout"], w.k_local, w.period, w.S,
+               w.mode, dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"], dalpha=bufs["dalpha"],
+               workspace=bufs["ws"], stream=stream)
+
+    def dec():
+        pa.decode(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, out=out,
+                  lse=lse, stream=stream)
+
+    if w.decode:
+        phases = [("pi_attn_decode", dec, 1)]
+    else:
+        # the backward is two kernels (query-major dq pass, key-major dk/dv pass) on either path
+        phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 2)] if w.backward else [])
+    return inp, d, out, lse, bufs, phases
+
+
+def time_steps(w, pa, dev, stream, phases, steps, warmup, sampler=None, world=1):
+    """CUDA-event times (ms) per phase of `steps` steps after `warmup` untimed ones, with the L2
+    flushed between steps (outside the events) when a step moves less than twice the L2.  The
+    timed steps are bracketed by a barrier (under torchrun) and a device synchronisation; the
+    clock sampler, if any, runs over them."""
+    wk = work(w, w.backward)
+    flush = wk["bytes"] < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, device=dev, dtype=torch.float32) if flush else None
+
+    def step(record=None):
+        for name, fn, _ in phases:
+            if record is not None:
+                record[name][0].record(stream)
+            fn()
+            if record is not None:
+                record[name][1].record(stream)
+
+    for _ in range(warmup):
+        if flush:
+            scratch.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if pa.status() != 0:
+        raise RuntimeError(f"{w.name}: device status word set during warm-up")
+    if sampler:
+        sampler.start()
+    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for n, _, _ in phases} for _ in range(steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(steps):
+        if flush:
+            scratch.zero_()
+        step(ev[k])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    status = pa.status()
+    if status != 0:
+        raise RuntimeError(f"{w.name}: device status word {status} after the timed region")
+    return {n: [e[n][0].elapsed_time(e[n][1]) for e in ev] for n, _, _ in phases}
+
+
+def config_numbers(w, per_phase, steps):
+    """The metric's numbers for one workload from its per-phase times."""
+    wk = work(w, w.backward)
+    total_ms = sum(sum(v) for v in per_phase.values())
+    tokens = w.B if w.decode else w.B * w.N
+    roof = roofline_of(w, wk, per_phase)
+    return {"workload": f"{w.name}: {w.description}", "dtype": w.dtype,
+            "ms_per_step": total_ms / steps, "tokens_per_s": tokens * steps / (total_ms / 1e3),
+            "useful_tflops": wk["flops"] * steps / (total_ms / 1e3) / 1e12,
+            "per_phase_ms": {n: statistics.mean(v) for n, v in per_phase.items()},
+            "roofline": {k: roof[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                               "t_roof_us", "kernel_us", "peak_source")},
+            "steps": steps}
+
+
+def other_configs(args, pa, dev, stream, names):
+    """The metric's other configurations, each timed in this process after the headline; a step
+    is the forward (C5: forward and backward), as for the headline."""
+    res = {}
+    for name in names:
+        w = WORKLOADS[name]
+        phases = setup_workload(w, pa, dev, stream)[5]
+        per_phase = time_steps(w, pa, dev, stream, phases, args.per_config_steps, 5)
+        res[name] = config_numbers(w, per_phase, args.per_config_steps)
+        del phases
+        torch.cuda.empty_cache()
+    return res
+
+
+def gpu_arm(args, w, rank, world, local_rank):
+    import structured_sparse_long_gb300 as pa
+    from structured_sparse_long_gb300 import build as pbuild
+
+    if rank == 0 or not os.path.exists(pbuild.LIB_PATH):
+        pbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pa.load()
+    stream = torch.cuda.current_stream(dev)
+
+    inp, d, out, lse, bufs, phases = setup_workload(w, pa, dev, stream)
+    wk = work(w, w.backward)
+    flush = wk["bytes"] < 2 * L2_BYTES
+    l2_note = ("L2 flushed between steps (write of a 2x L2 buffer outside the timed events)"
+               if flush else f"inputs larger than L2 ({wk['bytes'] / 1e6:.0f} MB moved per step)")
+
+    def step():
+        for _, fn, _ in phases:
+            fn()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    per_phase = time_steps(w, pa, dev, stream, phases, args.steps, args.warmup, sampler=sampler,
+                           world=world)
+    clocks = sampler.stop() if sampler else None
+    step_ms = [sum(per_phase[n][k] for n, _, _ in phases) for k in range(args.steps)]
+    total_ms = sum(step_ms)
+    total_ms = reduce_max(total_ms, world, dev if args.backend == "nccl" else "cpu")
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = (w.B if w.decode else w.B * w.N) * world
+    value = tokens_per_step * args.steps / (total_ms / 1e3)
+    tflops = wk["flops"] * world * args.steps / (total_ms / 1e3) / 1e12
+
+    # dominant kernel roofline (forward kernel: the whole step for the forward workloads)
+    roofline = roofline_of(w, wk, per_phase)
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -544,19 +601,25 @@ def gpu_arm(args, w, rank, world, local_rank):
 
     if rank != 0:
         return
+    per_config = None
+    if w.name == "C4" and not args.no_per_config:  # the metric's other configurations
+        per_config = {"C4": config_numbers(w, per_phase, args.steps)}
+        per_config.update(other_configs(args, pa, dev, stream, ("C1", "C2", "C3", "C5")))
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         tps, cores, desc = cpu_baseline(w, target_s=args.cpu_seconds)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded torch.Generator, shapes of the workload)",
             "config": config_block(w, l2_note), "useful_tflops": tflops,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * sum(n for _, _, n in phases),
             "clocks": clocks, "per_phase_ms": {n: statistics.mean(v) for n, v in per_phase.items()},
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
 
 
@@ -571,6 +634,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="the default C4 run also times C1, C2, C3 and C5; this skips them")
+    ap.add_argument("--per-config-steps", type=int, default=30)
     ap.add_argument("--seq", type=int, default=0,
                     help="override the sequence length N (smaller cases for profiler captures)")
     args = ap.parse_args()

@@ -115,22 +115,27 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
 
 /*
  * pi_attn_fwd_gated -- pi_attn_fwd with the gate fused into the same launch
- * ("pi-Attention" page, section 2.3: a light per-token, per-head network produces
- * alpha from the input content).  Reading of the network: a one-layer logistic
- * gate on the head's query,
- *     alpha_{b,h,i} = 1 / (1 + exp(-(q_{b,h,i} . gate_w[h] + gate_b[h]))),
+ * ("pi-Attention" page, section 2.3: a light neural network (MLP) produces alpha
+ * per token and per head from the input content).  Reading of the network: one
+ * hidden layer of PI_ATTN_GATE_HIDDEN units with a ReLU on the head's query, and
+ * a logistic output:
+ *     hid_f = max(0, sum_t gate_w1[h][f][t] q_{b,h,i,t} + gate_b1[h][f]),
+ *     alpha_{b,h,i} = 1 / (1 + exp(-(sum_f gate_w2[h][f] hid_f + gate_b2[h]))),
  * computed in fp32 from the bf16 query row the kernel has already staged, then
  * used exactly as pi_attn_fwd uses its alpha input.
- *   gate_w [H, d] fp32 (16-byte aligned), gate_b [H] fp32, alpha_out [B, H, N] fp32
- *   (may be NULL; receives the gate's alpha, e.g. for pi_attn_bwd, whose dalpha is then
- *   the gradient with respect to these values).  mode: pi or bidirectional (ECP:
- *   PI_ERR_UNSUPPORTED); d: 64 or 128 (else PI_ERR_UNSUPPORTED).  Other arguments,
- *   layouts and errors as pi_attn_fwd.
+ *   gate_w1 [H, PI_ATTN_GATE_HIDDEN, d] fp32 (16-byte aligned), gate_b1 and gate_w2
+ *   [H, PI_ATTN_GATE_HIDDEN] fp32, gate_b2 [H] fp32; alpha_out [B, H, N] fp32 (may be
+ *   NULL; receives the gate's alpha, e.g. for pi_attn_bwd, whose dalpha is then the
+ *   gradient with respect to these values; the gate's own weight gradients follow
+ *   from it by the chain rule on the caller's side).  mode: pi or bidirectional
+ *   (ECP: PI_ERR_UNSUPPORTED); d: 64 or 128 (else PI_ERR_UNSUPPORTED).  Other
+ *   arguments, layouts and errors as pi_attn_fwd.
  */
-int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w,
-                      const float *gate_b, int B, int H, int Hkv, int N, int d, int k_local,
-                      int period, int S, int mode, void *out, float *lse, float *alpha_out,
-                      void *stream);
+#define PI_ATTN_GATE_HIDDEN 8
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w1,
+                      const float *gate_b1, const float *gate_w2, const float *gate_b2, int B,
+                      int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
+                      void *out, float *lse, float *alpha_out, void *stream);
 
 /*
  * pi_attn_bwd_workspace_size -- bytes of device workspace pi_attn_bwd needs
@@ -152,8 +157,10 @@ size_t pi_attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  *   of each KV group) bf16; dalpha [B,H,N] fp32 (may be NULL; zero in ECP mode),
  *   computed as dalpha_i = -(sum_{j in P(i)} dz_ij) / (alpha_i (1 - alpha_i)),
  *   which equals sum_L dz/alpha - sum_P dz/(1-alpha) because every softmax row
- *   of dz sums to zero; it is undefined for alpha_i in {0, 1} when P(i) is not
- *   empty.  dz_ij = p_ij (dout_i . v_j - D_i), D_i = sum_j p_ij (dout_i . v_j).
+ *   of dz sums to zero; where alpha_i is exactly 0 or 1 (one prior is -inf, a
+ *   saturated gate) dalpha_i is 0, so that a gate whose fp32 sigmoid rounds to
+ *   1 passes no NaN upstream.  dz_ij = p_ij (dout_i . v_j - D_i),
+ *   D_i = sum_j p_ij (dout_i . v_j).
  *   workspace: device buffer of at least pi_attn_bwd_workspace_size() bytes,
  *   owned by the caller, contents ignored on entry.  Deterministic.
  */

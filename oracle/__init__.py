@@ -61,7 +61,7 @@ def _load():
         lib.oracle_fwd.restype = I
         lib.oracle_bwd.argtypes = [P, P, P, I, P, P, L, L, L, L, L, L, L, I, I, P, P, P, P]
         lib.oracle_bwd.restype = I
-        lib.oracle_gate.argtypes = [P, I, P, P, L, L, L, L, P]
+        lib.oracle_gate.argtypes = [P, I, P, P, P, P, L, L, L, L, L, P]
         lib.oracle_gate.restype = None
         _lib = lib
         return lib
@@ -166,27 +166,32 @@ def bwd(q, k, v, alpha, dout, k_local, period, S, mode):
     return dq, dk, dv, dal
 
 
-def gate(q, w, c):
-    """Gate alpha [B,H,N] (float64): 1 / (1 + exp(-(q . w_h + c_h))) for every query row.
+def gate(q, w1, b1, w2, b2):
+    """Gate alpha [B,H,N] (float64) through the per-head MLP of one hidden layer:
+    hid = max(0, W1_h q + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h))).
 
-    q [B,H,N,d] (bf16, fp32 or fp64), w [H,d] and c [H] (any float type; taken as fp64).
-    The pi-Attention page, 2.3, names a light per-token, per-head network producing alpha
-    from the input content; this is its one-layer reading on the head's query.
+    q [B,H,N,d] (bf16, fp32 or fp64); W1 [H,F,d], b1 [H,F], w2 [H,F], b2 [H] (any float type;
+    taken as fp64).  The pi-Attention page, 2.3, names a light network (MLP) per token and per
+    head producing alpha from the input content; the head's query is its input here.
     """
     lib = _load()
     qa, dt = _as_raw(q)
     B, H, N, d = qa.shape
-    wa = np.ascontiguousarray(_np64(w).reshape(H, d))
-    ca = np.ascontiguousarray(_np64(c).reshape(H))
+    w1a = np.ascontiguousarray(_np64(w1))
+    F = w1a.shape[1]
+    w1a = w1a.reshape(H, F, d)
+    b1a = np.ascontiguousarray(_np64(b1).reshape(H, F))
+    w2a = np.ascontiguousarray(_np64(w2).reshape(H, F))
+    b2a = np.ascontiguousarray(_np64(b2).reshape(H))
     alpha = np.zeros((B, H, N), dtype=np.float64)
-    lib.oracle_gate(_ptr(qa), dt, _ptr(wa), _ptr(ca), B, H, N, d, _ptr(alpha))
+    lib.oracle_gate(_ptr(qa), dt, _ptr(w1a), _ptr(b1a), _ptr(w2a), _ptr(b2a), B, H, N, d, F, _ptr(alpha))
     return alpha
 
 
-def fwd_gated(q, k, v, w, c, k_local, period, S, mode, rows=None):
+def fwd_gated(q, k, v, gate_weights, k_local, period, S, mode, rows=None):
     """Forward with alpha from the gate (rounded to fp32, the precision the forward takes alpha
-    in).  Returns (out, lse, alpha) with alpha the fp64 gate."""
-    alpha = gate(q, w, c)
+    in); gate_weights = (W1, b1, w2, b2).  Returns (out, lse, alpha) with alpha the fp64 gate."""
+    alpha = gate(q, *gate_weights)
     out, lse = fwd(q, k, v, alpha.astype(np.float32), k_local, period, S, mode, rows=rows)
     return out, lse, alpha
 

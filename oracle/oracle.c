@@ -39,12 +39,14 @@
  *   D_i = dout_i . out_i ;  dz_ij = p_ij (dout_i . v_j - D_i)
  *   dq_i = sum_j dz_ij k_j / sqrt(d);  dk_j = sum_{h in group, i} dz_ij q_i / sqrt(d)
  *   dv_j = sum_{h in group, i} p_ij dout_i
- *   dalpha_i = sum_{j local} dz_ij / alpha_i - sum_{j skip} dz_ij / (1 - alpha_i)
+ *   dalpha_i = sum_{j local} dz_ij / alpha_i - sum_{j skip} dz_ij / (1 - alpha_i),
+ *   taken as 0 where alpha_i is 0 or 1 (there one prior is -inf: a saturated gate)
  *
- * Gate (same page, 2.3: a light per-token, per-head network producing alpha
- * from the input content).  Reading: a one-layer logistic gate on the head's
- * query, alpha_{b,h,i} = 1 / (1 + exp(-(q_{b,h,i} . w_h + c_h))), w [H, d],
- * c [H]; the query projection is the network's first layer.
+ * Gate (same page, 2.3: a light neural network (MLP) producing alpha per token and
+ * per head from the input content).  Reading: one hidden layer of F units with a
+ * ReLU on the head's query, the output through a logistic function:
+ *   hid_f = max(0, sum_t W1[h][f][t] q_t + b1[h][f]),  f = 0 .. F-1,
+ *   alpha_{b,h,i} = 1 / (1 + exp(-(sum_f w2[h][f] hid_f + b2[h]))).
  *
  * Inputs may be fp64, fp32 or raw bf16 bits; bf16 is widened exactly.  All
  * arithmetic is fp64.  Parallel over query rows with OpenMP.
@@ -288,9 +290,11 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
                         }
                     }
                     if (dalpha) {
+                        /* At alpha = 0 or 1 one prior is -inf and its weights are exactly 0; the
+                           derivative there is taken as 0 (a saturated gate passes no gradient). */
                         double g_a = 0.0;
-                        if (mode != MODE_ECP) {
-                            double a = alpha ? (double)alpha[((size_t)b * H + h) * N + i] : 1.0;
+                        double a = alpha ? (double)alpha[((size_t)b * H + h) * N + i] : 1.0;
+                        if (mode != MODE_ECP && a > 0.0 && a < 1.0) {
                             g_a = sum_local / a - sum_skip / (1.0 - a);
                             if (sum_skip == 0.0) g_a = sum_local / a;
                         }
@@ -306,16 +310,20 @@ int oracle_bwd(const void *q, const void *k, const void *v, int dt, const float 
 }
 
 /*
- * Gate: alpha [B, H, N] fp64 from q [B, H, N, d] (any input dtype), w [H, d] and c [H]
- * (fp64).  alpha = 1 / (1 + exp(-(q . w_h + c_h))).
+ * Gate: alpha [B, H, N] fp64 from q [B, H, N, d] (any input dtype) through the MLP above:
+ * W1 [H, F, d], b1 [H, F], w2 [H, F], b2 [H] (fp64).
  */
-void oracle_gate(const void *q, int dt, const double *w, const double *c, long B, long H, long N,
-                 long d, double *alpha) {
+void oracle_gate(const void *q, int dt, const double *w1, const double *b1, const double *w2,
+                 const double *b2, long B, long H, long N, long d, long F, double *alpha) {
 #pragma omp parallel for schedule(static)
     for (long row = 0; row < B * H * N; ++row) {
         const long h = (row / N) % H;
-        double z = c[h];
-        for (long t = 0; t < d; ++t) z += ld(q, dt, (size_t)row * d + t) * w[h * d + t];
+        double z = b2[h];
+        for (long f = 0; f < F; ++f) {
+            double pre = b1[h * F + f];
+            for (long t = 0; t < d; ++t) pre += ld(q, dt, (size_t)row * d + t) * w1[(h * F + f) * d + t];
+            if (pre > 0.0) z += w2[h * F + f] * pre;
+        }
         alpha[row] = 1.0 / (1.0 + exp(-z));
     }
 }

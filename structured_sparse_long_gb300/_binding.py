@@ -69,7 +69,7 @@ def load() -> ctypes.CDLL:
         lib.pi_attn_debug_trace.restype = I
         lib.pi_attn_decode.argtypes = [P, P, P, P] + [I] * 9 + [P, P, P]
         lib.pi_attn_decode.restype = I
-        lib.pi_attn_fwd_gated.argtypes = [P, P, P, P, P] + [I] * 9 + [P, P, P, P]
+        lib.pi_attn_fwd_gated.argtypes = [P, P, P, P, P, P, P] + [I] * 9 + [P, P, P, P]
         lib.pi_attn_fwd_gated.restype = I
         for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
                      "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
@@ -109,6 +109,14 @@ def _expect(t: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _expect_like(t, name, ref, dtype, shape):
+    """A caller-supplied output buffer: a contiguous CUDA tensor of the given dtype and shape on
+    the device of `ref` (the kernels store into it with TMA maps sized from the inputs)."""
+    _expect(t, name, dtype, shape)
+    if t.device != ref.device:
+        raise ValueError(f"{name} must be on {ref.device}, got {t.device}")
+
+
 def _sizes(q, k):
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B,H,N,d] and k [B,Hkv,N,d]")
@@ -142,17 +150,23 @@ def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
     return out, lse
 
 
-def fwd_gated(q, k, v, gate_w, gate_b, k_local: int, period: int, S: int, mode: int = MODE_PI,
+GATE_HIDDEN = 8  # PI_ATTN_GATE_HIDDEN in include/pi_attn.h
+
+
+def fwd_gated(q, k, v, gate, k_local: int, period: int, S: int, mode: int = MODE_PI,
               out=None, lse=None, alpha_out=None, stream=None):
-    """pi_attn_fwd_gated (bf16, d 64 or 128): the forward with the gate
-    alpha = 1 / (1 + exp(-(q . gate_w[h] + gate_b[h]))) computed in the same launch.
-    gate_w [H, d] and gate_b [H] fp32.  Returns (out, lse, alpha)."""
+    """pi_attn_fwd_gated (bf16, d 64 or 128): the forward with the gate computed in the same
+    launch by the per-head MLP hid = max(0, W1_h q + b1_h), alpha = 1/(1 + exp(-(w2_h . hid + b2_h))).
+    gate = (W1 [H, 8, d], b1 [H, 8], w2 [H, 8], b2 [H]), fp32.  Returns (out, lse, alpha)."""
     B, H, Hkv, N, d = _sizes(q, k)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _expect(t, n, torch.bfloat16)
     _expect(v, "v", torch.bfloat16, k.shape)
-    _expect(gate_w, "gate_w", torch.float32, (H, d))
-    _expect(gate_b, "gate_b", torch.float32, (H,))
+    w1, b1, w2, b2 = gate
+    _expect(w1, "gate_w1", torch.float32, (H, GATE_HIDDEN, d))
+    _expect(b1, "gate_b1", torch.float32, (H, GATE_HIDDEN))
+    _expect(w2, "gate_w2", torch.float32, (H, GATE_HIDDEN))
+    _expect(b2, "gate_b2", torch.float32, (H,))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -163,8 +177,8 @@ def fwd_gated(q, k, v, gate_w, gate_b, k_local: int, period: int, S: int, mode: 
     _expect(lse, "lse", torch.float32, (B, H, N))
     _expect(alpha_out, "alpha_out", torch.float32, (B, H, N))
     lib = load()
-    rc = lib.pi_attn_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_w), _ptr(gate_b), B, H, Hkv, N, d,
-                               k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(alpha_out),
+    rc = lib.pi_attn_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), B, H, Hkv,
+                               N, d, k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(alpha_out),
                                _stream(stream))
     _check("pi_attn_fwd_gated", rc)
     return out, lse, alpha_out
@@ -199,6 +213,21 @@ def bwd_workspace_size(B, H, Hkv, N, d) -> int:
     return int(load().pi_attn_bwd_workspace_size(B, H, Hkv, N, d))
 
 
+def _grad_buffers(q, k, v, dq, dk, dv, dalpha):
+    """The gradient outputs of the backward: the caller's buffers, checked, or new ones."""
+    B, H, N = q.shape[0], q.shape[1], q.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dalpha is None:
+        dalpha = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _expect_like(dq, "dq", q, q.dtype, q.shape)
+    _expect_like(dk, "dk", q, q.dtype, k.shape)
+    _expect_like(dv, "dv", q, q.dtype, v.shape)
+    _expect_like(dalpha, "dalpha", q, torch.float32, (B, H, N))
+    return dq, dk, dv, dalpha
+
+
 def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode: int = MODE_PI,
         dq=None, dk=None, dv=None, dalpha=None, workspace=None, stream=None):
     """pi_attn_bwd (bf16) / pi_attn_bwd_f32, chosen by q.dtype. Returns (dq, dk, dv, dalpha)."""
@@ -211,14 +240,13 @@ def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode:
     _expect(lse, "lse", torch.float32, (B, H, N))
     if alpha is not None:
         _expect(alpha, "alpha", torch.float32, (B, H, N))
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if dalpha is None:
-        dalpha = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    dq, dk, dv, dalpha = _grad_buffers(q, k, v, dq, dk, dv, dalpha)
     nbytes = bwd_workspace_size(B, H, Hkv, N, d)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+    _expect_like(workspace, "workspace", q, torch.uint8, None)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace must hold {nbytes} bytes, got {workspace.numel()}")
     lib = load()
     fn = {torch.bfloat16: lib.pi_attn_bwd, torch.float32: lib.pi_attn_bwd_f32}.get(dt)
     if fn is None:
@@ -242,11 +270,7 @@ def bwd_noalloc(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: in
     _expect(lse, "lse", torch.float32, (B, H, N))
     if alpha is not None:
         _expect(alpha, "alpha", torch.float32, (B, H, N))
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if dalpha is None:
-        dalpha = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    dq, dk, dv, dalpha = _grad_buffers(q, k, v, dq, dk, dv, dalpha)
     rc = load().pi_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse),
                                     _ptr(dout), B, H, Hkv, N, d, k_local, period, S, mode,
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _stream(stream))

@@ -4,6 +4,7 @@
 // launched, picks the kernel for the dtype and head size, and launches it on the
 // caller's stream.  No entry point allocates device memory: the status word is
 // a static __device__ variable, one per device.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -18,16 +19,20 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bound on every device-sid
 constexpr int kMaxDevices = 64;
 constexpr int kDebugMaxN = 2048;
 
+// Device address of g_status_word for the current device, looked up once per device (two
+// threads may both look it up the first time; they store the same address).
 int *status_word() {
-    static int *cache[kMaxDevices] = {};
+    static std::atomic<int *> cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<int *>(p);
+    int *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_status_word) != cudaSuccess) return nullptr;
+        p = static_cast<int *>(a);
+        cache[dev].store(p, std::memory_order_release);
     }
-    return cache[dev];
+    return p;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -128,18 +133,19 @@ static __device__ __align__(256) float g_noalloc_scratch[PI_ATTN_NOALLOC_MAX_ROW
 
 namespace {
 
-// Device address of g_noalloc_scratch for the current device, looked up once per device.
+// Device address of g_noalloc_scratch for the current device, looked up once per device (two
+// threads may both look it up the first time; they store the same address).
 float *noalloc_scratch() {
-    static float *cache[kMaxDevices] = {};
+    static std::atomic<float *> cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!cache[dev]) {
-        float *p = nullptr;
+    float *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_scratch) != cudaSuccess)
             return nullptr;
-        cache[dev] = p;
+        cache[dev].store(p, std::memory_order_release);
     }
-    return cache[dev];
+    return p;
 }
 
 }  // namespace
@@ -160,16 +166,19 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
                    0, nullptr, nullptr, nullptr, nullptr);
 }
 
-int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w,
-                      const float *gate_b, int B, int H, int Hkv, int N, int d, int k_local, int period,
-                      int S, int mode, void *out, float *lse, float *alpha_out, void *stream) {
-    if (!gate_w || !gate_b) return PI_ERR_NULL;
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w1,
+                      const float *gate_b1, const float *gate_w2, const float *gate_b2, int B, int H,
+                      int Hkv, int N, int d, int k_local, int period, int S, int mode, void *out,
+                      float *lse, float *alpha_out, void *stream) {
+    if (!gate_w1 || !gate_b1 || !gate_w2 || !gate_b2) return PI_ERR_NULL;
     // the gate is the pi mode's (causal or bidirectional); ECP has no prior to weight
     if (mode != PI_MODE_PI && mode != PI_MODE_PI_BIDIR) return PI_ERR_UNSUPPORTED;
-    const int rc = validate_fwd(q, k, v, gate_b, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
+    const int rc = validate_fwd(q, k, v, gate_b2, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
     if (rc != PI_OK) return rc;
     if (d != 64 && d != 128) return PI_ERR_UNSUPPORTED;  // the tensor-core forward only
-    if (!aligned(gate_w, 16) || !aligned(gate_b, 4) || (alpha_out && !aligned(alpha_out, 4))) return PI_ERR_ALIGN;
+    if (!aligned(gate_w1, 16) || !aligned(gate_b1, 4) || !aligned(gate_w2, 4) || !aligned(gate_b2, 4) ||
+        (alpha_out && !aligned(alpha_out, 4)))
+        return PI_ERR_ALIGN;
     int *status = status_word();
     if (!status) return PI_ERR_CUDA;
     pi::LaunchFwd L;
@@ -179,7 +188,7 @@ int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *
     L.fp32 = false; L.dbg = 0; L.cnt = nullptr; L.isum = nullptr; L.lse_in = nullptr; L.P = nullptr;
     L.trace = nullptr; L.n_trace = 0;
     L.status = status; L.timeout_ns = kWaitTimeoutNs;
-    L.gate_w = gate_w; L.gate_b = gate_b; L.alpha_out = alpha_out;
+    L.gate_w1 = gate_w1; L.gate_b1 = gate_b1; L.gate_w2 = gate_w2; L.gate_b2 = gate_b2; L.alpha_out = alpha_out;
     return map_cuda(pi::launch_fwd_tc(L, static_cast<cudaStream_t>(stream)));
 }
 

@@ -171,7 +171,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     cw.m_first = 1;
     cw.n_back = 0;
     if (s.mode != kModeEcp && s.S > 0) {
-        cw.m_first = max(1, s.k_local / s.period + 1);
+        cw.m_first = first_skip_multiple(s);
         const int m_last = min(s.S, (p0 + R - 1) / s.period);  // some row has i - m*period >= 0
         cw.n_back = max(0, m_last - cw.m_first + 1);
         n_skip_blocks = cw.n_back;
@@ -478,7 +478,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (args.dalpha) {
                 any_skip = any_skip && live;
                 args.dalpha[row_g] =
-                    (s.mode != kModeEcp && any_skip) ? -(skip_pdp - dsum * skip_p) / (al * (1.f - al)) : 0.f;
+                    (s.mode != kModeEcp && any_skip && al > 0.f && al < 1.f)
+                        ? -(skip_pdp - dsum * skip_p) / (al * (1.f - al)) : 0.f;  // saturated gate: 0
             }
         }
     }
@@ -497,14 +498,14 @@ static cudaError_t launch_dq(const CUtensorMap &mq, const CUtensorMap &mg, const
                             const CUtensorMap &mv, const CUtensorMap &mdq, const DqArgs &a,
                             unsigned grid, cudaStream_t st) {
     constexpr int smem = CfgQ<D>::SMEM_BYTES;
-    static int configured_device = -1;
+    static PerDeviceOnce configured;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
+    if (configured.needed(dev)) {
         cudaError_t e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured.mark(dev);
     }
     bwd_dq_tc_kernel<D><<<grid, NUM_THREADS, smem, st>>>(mq, mg, mk, mv, mdq, a);
     return cudaGetLastError();
@@ -628,7 +629,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     kw.n_fwd = 0;
     kw.n_skip = 0;
     if (s.mode != kModeEcp && s.S > 0) {
-        kw.m_first = max(1, s.k_local / s.period + 1);
+        kw.m_first = first_skip_multiple(s);
         // multiples whose first skip query j0 + m*period is inside the sequence
         const int m_last = min(s.S, (s.N - 1 - kw.j0) / s.period);
         kw.n_fwd = max(0, m_last - kw.m_first + 1);
@@ -917,14 +918,14 @@ static cudaError_t launch_dkdv(const CUtensorMap &mk, const CUtensorMap &mv, con
                               const CUtensorMap &mgc, const CUtensorMap &mdk, const CUtensorMap &mdv,
                               const DkvArgs &a, unsigned grid, cudaStream_t st) {
     constexpr int smem = CfgK<D>::SMEM_BYTES;
-    static int configured_device = -1;
+    static PerDeviceOnce configured;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
+    if (configured.needed(dev)) {
         cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured.mark(dev);
     }
     bwd_dkdv_tc_kernel<D><<<grid, NUM_THREADS, smem, st>>>(mk, mv, mqc, mgc, mdk, mdv, a);
     return cudaGetLastError();

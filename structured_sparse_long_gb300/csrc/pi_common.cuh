@@ -74,6 +74,14 @@ __host__ __device__ __forceinline__ int band_last_query(int j, int N, int mode, 
     return hi > N - 1 ? N - 1 : (int)hi;
 }
 
+// Smallest skip multiple m with m*period > k_local, at most S + 1 (no skip key at all then);
+// computed in 64 bits, as k_local may be as large as INT_MAX.
+__host__ __device__ __forceinline__ int first_skip_multiple(const Shape &s) {
+    if (s.period <= 0) return 1;
+    const long long m = (long long)s.k_local / s.period + 1;
+    return (int)(m < (long long)s.S + 1 ? m : (long long)s.S + 1);
+}
+
 // Skip multiple m contributes a key distinct from the band iff m*period > k_local.
 __host__ __device__ __forceinline__ bool skip_in_use(int m, int period, int k_local) {
     return (long long)m * period > (long long)k_local;

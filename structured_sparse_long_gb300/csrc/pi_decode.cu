@@ -340,7 +340,7 @@ cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st) {
     a.m_first = 1;
     int n_skip = 0;
     if (s.mode != kModeEcp && s.S > 0) {
-        a.m_first = s.k_local / s.period + 1;
+        a.m_first = first_skip_multiple(s);
         const int m_last = min(s.S, i / s.period);
         n_skip = max(0, m_last - a.m_first + 1);
     }

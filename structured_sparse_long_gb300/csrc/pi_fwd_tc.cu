@@ -233,9 +233,12 @@ struct TcArgs {
     float *P;
     long long *trace;  // DBG 3: clock64() stamps, kTraceSlots per traced CTA
     int n_trace;       // DBG 3: CTAs 0 .. n_trace-1 are traced
-    const float *gate_w;  // fused gate (or null): alpha = 1 / (1 + exp(-(q_i . gate_w[h] + gate_b[h])))
-    const float *gate_b;
-    float *alpha_out;     // [B, H, N] the gate's alpha (may be null)
+    // fused gate (or null): hid = max(0, W1_h q_i + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h)))
+    const float *gate_w1;  // [H, kGateHidden, d]
+    const float *gate_b1;  // [H, kGateHidden]
+    const float *gate_w2;  // [H, kGateHidden]
+    const float *gate_b2;  // [H]
+    float *alpha_out;      // [B, H, N] the gate's alpha (may be null)
 };
 
 // Trace layout (DBG 3: one block per CTA), slots per CTA: 0 entry, 1 set-up done, 2 Q issued,
@@ -326,13 +329,19 @@ __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc
 
 // This row of a Q tile (staged in shared memory, 128B-swizzled) into TMEM lane (the calling
 // thread's), columns Q_COL + w holding the bf16 pair (q[2w], q[2w+1]): the A operand layout
-// of the S products.  Returns the fused gate's logit q . w_h + c_h when wh is not null ("pi-
-// Attention" page, 2.3: a per-token, per-head logistic gate), which reads the same words.  One
-// out-of-line copy: it runs once per block.
-template <int D>
-static __device__ __noinline__ float copy_q_row(const uint8_t *qrow, int swz, uint32_t taddr, const float *wh,
-                                                float bias) {
-    float z0 = bias, z1 = 0.f;
+// of the S products.  When w1 is not null it also evaluates the fused gate's network ("pi-
+// Attention" page, 2.3: a light MLP per token and per head) on the same words: the hidden
+// pre-activations W1_h q + b1_h, then the output logit w2_h . max(0, .) + b2_h, returned.  The
+// weights of a warp's rows are one head's, so their loads are warp-uniform.  One out-of-line
+// copy: it runs once per block.
+template <int D, bool GATE>
+static __device__ __noinline__ float copy_q_row(const uint8_t *qrow, int swz, uint32_t taddr, const float *w1,
+                                                const float *b1, const float *w2, float b2) {
+    float pre[kGateHidden];
+    if (GATE) {
+#pragma unroll
+        for (int f = 0; f < kGateHidden; ++f) pre[f] = b1[f];
+    }
 #pragma unroll 1
     for (int dc = 0; dc < D / 64; ++dc) {
         uint32_t wq[32];
@@ -343,26 +352,39 @@ static __device__ __noinline__ float copy_q_row(const uint8_t *qrow, int swz, ui
             wq[4 * ch + 1] = u4.y;
             wq[4 * ch + 2] = u4.z;
             wq[4 * ch + 3] = u4.w;
-            if (wh) {
-                const float4 wa = *reinterpret_cast<const float4 *>(wh + dc * 64 + ch * 8);
-                const float4 wb = *reinterpret_cast<const float4 *>(wh + dc * 64 + ch * 8 + 4);
-                z0 = fmaf(__uint_as_float(u4.x << 16), wa.x, z0);
-                z1 = fmaf(__uint_as_float(u4.x & 0xffff0000u), wa.y, z1);
-                z0 = fmaf(__uint_as_float(u4.y << 16), wa.z, z0);
-                z1 = fmaf(__uint_as_float(u4.y & 0xffff0000u), wa.w, z1);
-                z0 = fmaf(__uint_as_float(u4.z << 16), wb.x, z0);
-                z1 = fmaf(__uint_as_float(u4.z & 0xffff0000u), wb.y, z1);
-                z0 = fmaf(__uint_as_float(u4.w << 16), wb.z, z0);
-                z1 = fmaf(__uint_as_float(u4.w & 0xffff0000u), wb.w, z1);
+            if (GATE) {
+                const float qv[8] = {__uint_as_float(u4.x << 16), __uint_as_float(u4.x & 0xffff0000u),
+                                     __uint_as_float(u4.y << 16), __uint_as_float(u4.y & 0xffff0000u),
+                                     __uint_as_float(u4.z << 16), __uint_as_float(u4.z & 0xffff0000u),
+                                     __uint_as_float(u4.w << 16), __uint_as_float(u4.w & 0xffff0000u)};
+#pragma unroll
+                for (int f = 0; f < kGateHidden; ++f) {
+                    const float *wr = w1 + f * D + dc * 64 + ch * 8;
+                    const float4 wa = *reinterpret_cast<const float4 *>(wr);
+                    const float4 wb = *reinterpret_cast<const float4 *>(wr + 4);
+                    pre[f] = fmaf(qv[0], wa.x, pre[f]);
+                    pre[f] = fmaf(qv[1], wa.y, pre[f]);
+                    pre[f] = fmaf(qv[2], wa.z, pre[f]);
+                    pre[f] = fmaf(qv[3], wa.w, pre[f]);
+                    pre[f] = fmaf(qv[4], wb.x, pre[f]);
+                    pre[f] = fmaf(qv[5], wb.y, pre[f]);
+                    pre[f] = fmaf(qv[6], wb.z, pre[f]);
+                    pre[f] = fmaf(qv[7], wb.w, pre[f]);
+                }
             }
         }
         tmem_st16(taddr + dc * 32, wq);
         tmem_st16(taddr + dc * 32 + 16, wq + 16);
     }
-    return z0 + z1;
+    float z = b2;
+    if (GATE) {
+#pragma unroll
+        for (int f = 0; f < kGateHidden; ++f) z = fmaf(w2[f], fmaxf(pre[f], 0.f), z);
+    }
+    return z;
 }
 
-template <int D, int DBG>
+template <int D, int DBG, bool GATE>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -671,13 +693,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const bool row_ok = i < s.N;
             const long long row_g = ((long long)bd.b * s.H + h) * s.N + i;
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), (uint32_t)(kb & 1), wc))) return false;
-            const float *wh = args.gate_w ? args.gate_w + (size_t)h * D : nullptr;
-            const float z = copy_q_row<D>(smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL, wh,
-                                          wh ? args.gate_b[h] : 0.f);
+            constexpr bool gated = GATE;
+            const float z = copy_q_row<D, GATE>(
+                smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL,
+                gated ? args.gate_w1 + (size_t)h * kGateHidden * D : nullptr,
+                gated ? args.gate_b1 + h * kGateHidden : nullptr, gated ? args.gate_w2 + h * kGateHidden : nullptr,
+                gated ? args.gate_b2[h] : 0.f);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_QT));
-            if (wh) {
+            if (gated) {
                 al_out = 1.f / (1.f + __expf(-z));
                 if (args.alpha_out && row_ok) args.alpha_out[row_g] = al_out;
             } else {
@@ -923,35 +948,35 @@ __global__ void wait_timeout_probe_kernel(int *status, uint64_t timeout_ns) {
 
 // ------------------------------------------------------------------ host side
 
-template <int D, int DBG>
+template <int D, int DBG, bool GATE = false>
 static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const CUtensorMap &mo, const TcArgs &a, unsigned grid, cudaStream_t st) {
     constexpr int smem = Cfg<D>::SMEM_BYTES;
-    static int configured_device = -1;
+    static PerDeviceOnce configured;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, DBG>,
+    if (configured.needed(dev)) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, DBG, GATE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured.mark(dev);
     }
-    fwd_tc_kernel<D, DBG><<<grid, NUM_THREADS, smem, st>>>(mq, mk, mv, mo, a);
+    fwd_tc_kernel<D, DBG, GATE><<<grid, NUM_THREADS, smem, st>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
 }
 
 // Streaming multiprocessors of the current device (looked up once per device).
 static int sm_count() {
     constexpr int kMaxDev = 64;
-    static int cache[kMaxDev] = {};
+    static std::atomic<int> cache[kMaxDev];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 }  // namespace tc
@@ -968,11 +993,7 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
-    int m_first = 1;
-    if (s.mode != kModeEcp && s.S > 0) {  // smallest m with m*period > k, at most S + 1
-        const long long m = (long long)s.k_local / s.period + 1;
-        m_first = (int)(m < (long long)s.S + 1 ? m : (long long)s.S + 1);
-    }
+    const int m_first = (s.mode != kModeEcp && s.S > 0) ? first_skip_multiple(s) : 1;
     const int nqb = (s.N + R - 1) / R, ngrp = s.H / GP;
     const long long nb64 = (long long)nqb * ngrp * s.B;
     if (nb64 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -980,12 +1001,19 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     const int cpb_log2 = (R == 128) ? 2 : (R == 64) ? 1 : 0;
     TcArgs a{L.alpha, L.lse, s, GP, m_first, nqb, ngrp, R, cpb_log2, make_fastdiv(nqb), make_fastdiv(ngrp),
              make_fastdiv(G), make_fastdiv(s.S > 0 && s.period > 0 ? s.period : 1), n_blocks, L.status,
-             L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P, L.trace, L.n_trace, L.gate_w, L.gate_b, L.alpha_out};
+             L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P, L.trace, L.n_trace, L.gate_w1, L.gate_b1, L.gate_w2,
+             L.gate_b2, L.alpha_out};
     // The forward runs persistent, two CTAs per SM; the debug modes take one CTA per block.
     unsigned grid = (unsigned)n_blocks;
     if (L.dbg == 0) {
         const int resident = 2 * sm_count();
         if (resident > 0 && resident < n_blocks) grid = (unsigned)resident;
+    }
+    if (L.gate_w1) {  // the fused gate: the forward only
+        if (L.dbg != 0) return cudaErrorInvalidValue;
+        if (s.d == 64) return launch<64, 0, true>(mq, mk, mv, mo, a, grid, st);
+        if (s.d == 128) return launch<128, 0, true>(mq, mk, mv, mo, a, grid, st);
+        return cudaErrorInvalidValue;
     }
     if (s.d == 64) {
         if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, grid, st);

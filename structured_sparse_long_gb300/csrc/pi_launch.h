@@ -1,12 +1,27 @@
 // pi_launch.h -- host-side launch descriptors shared by the C ABI and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "pi_common.cuh"
 
 namespace pi {
+
+constexpr int kGateHidden = 8;  // hidden units per head of the fused gate
+
+// A host-side set-up done once per device (devices 0-63; others redo it on every call).
+// Thread-safe: two threads may both do the set-up the first time, which is harmless.
+struct PerDeviceOnce {
+    std::atomic<unsigned long long> done{0};
+    bool needed(int dev) const {
+        return dev < 0 || dev >= 64 || !((done.load(std::memory_order_acquire) >> dev) & 1ull);
+    }
+    void mark(int dev) {
+        if (dev >= 0 && dev < 64) done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+    }
+};
 
 struct LaunchFwd {
     const void *q, *k, *v;
@@ -24,11 +39,14 @@ struct LaunchFwd {
     int n_trace;           // dbg 3: number of traced CTAs
     int *status;           // device status word
     uint64_t timeout_ns;   // bound on every device-side wait
-    // fused gate (tensor-core path): alpha = 1 / (1 + exp(-(q_i . gate_w[h] + gate_b[h]))) is
-    // computed in the kernel instead of read from alpha; alpha_out (may be null) receives it
-    const float *gate_w = nullptr;  // [H, d]
-    const float *gate_b = nullptr;  // [H]
-    float *alpha_out = nullptr;     // [B, H, N]
+    // fused gate (tensor-core path): alpha from the per-head MLP of one hidden layer,
+    // hid = max(0, W1_h q_i + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h))), computed in
+    // the kernel instead of read from alpha; alpha_out (may be null) receives it
+    const float *gate_w1 = nullptr;  // [H, kGateHidden, d]
+    const float *gate_b1 = nullptr;  // [H, kGateHidden]
+    const float *gate_w2 = nullptr;  // [H, kGateHidden]
+    const float *gate_b2 = nullptr;  // [H]
+    float *alpha_out = nullptr;      // [B, H, N]
 };
 
 struct LaunchBwd {

@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
     if (lane == 0) {
         a.Dws[row] = Drow;
         if (a.dalpha)
-            a.dalpha[row] = (s.mode != kModeEcp && any_skip) ? -sdz / (al * (1.f - al)) : 0.f;
+            a.dalpha[row] = (s.mode != kModeEcp && any_skip && al > 0.f && al < 1.f)
+                                ? -sdz / (al * (1.f - al)) : 0.f;  // saturated gate: 0
     }
 }
 

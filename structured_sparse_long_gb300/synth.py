@@ -161,10 +161,17 @@ def small_case(name="case", B=1, H=2, Hkv=2, N=300, d=64, k_local=40, period=64,
                     alpha, backward)
 
 
+GATE_HIDDEN = 8  # hidden units per head of the fused gate
+
+
 def gate_weights(H: int, d: int, seed: int):
-    """Synthetic weights of the fused gate: w [H, d] ~ N(0, 1/d) and c [H] ~ N(0, 1), fp32, so that
-    for unit-variance queries the gate logit q . w_h + c_h has about unit spread."""
+    """Synthetic weights of the fused gate's per-head MLP, fp32: W1 [H, 8, d] ~ N(0, 1/d) and
+    b1 [H, 8] ~ N(0, 1/4), so that for unit-variance queries the hidden pre-activations have
+    about unit spread; w2 [H, 8] ~ N(0, 2/8) and b2 [H] ~ N(0, 1), so that the output logit
+    spreads over about one unit and alpha covers (0, 1) without saturating."""
     gen = torch.Generator().manual_seed(seed)
-    w = torch.randn(H, d, generator=gen, dtype=torch.float32) / math.sqrt(d)
-    c = torch.randn(H, generator=gen, dtype=torch.float32)
-    return w, c
+    w1 = torch.randn(H, GATE_HIDDEN, d, generator=gen, dtype=torch.float32) / math.sqrt(d)
+    b1 = 0.5 * torch.randn(H, GATE_HIDDEN, generator=gen, dtype=torch.float32)
+    w2 = torch.randn(H, GATE_HIDDEN, generator=gen, dtype=torch.float32) * math.sqrt(2.0 / GATE_HIDDEN)
+    b2 = torch.randn(H, generator=gen, dtype=torch.float32)
+    return w1, b1, w2, b2

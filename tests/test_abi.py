@@ -91,15 +91,19 @@ def test_fwd_validation(lib, fn):
     assert fwd_call(lib, lse=A16 + 2, fn=fn) == PI_ERR_ALIGN
 
 
-def gated_call(lib, q=A16, gw=A16, gb=A16, B=1, H=2, Hkv=2, N=64, d=64, kl=8, per=16, S=1, mode=0,
-               out=A16, lse=A16, aout=A16):
-    return lib.pi_attn_fwd_gated(q, A16, A16, gw, gb, B, H, Hkv, N, d, kl, per, S, mode, out, lse, aout,
-                                 None)
+def gated_call(lib, q=A16, gw=A16, gb=A16, w2=A16, b2=A16, B=1, H=2, Hkv=2, N=64, d=64, kl=8, per=16,
+               S=1, mode=0, out=A16, lse=A16, aout=A16):
+    return lib.pi_attn_fwd_gated(q, A16, A16, gw, gb, w2, b2, B, H, Hkv, N, d, kl, per, S, mode, out, lse,
+                                 aout, None)
 
 
 def test_fwd_gated_validation(lib):
     assert gated_call(lib, gw=None) == PI_ERR_NULL
     assert gated_call(lib, gb=None) == PI_ERR_NULL
+    assert gated_call(lib, w2=None) == PI_ERR_NULL
+    assert gated_call(lib, b2=None) == PI_ERR_NULL
+    assert gated_call(lib, w2=A16 + 2) == PI_ERR_ALIGN
+    assert gated_call(lib, b2=A16 + 2) == PI_ERR_ALIGN
     assert gated_call(lib, q=None) == PI_ERR_NULL
     assert gated_call(lib, mode=1, kl=16, S=0) == PI_ERR_UNSUPPORTED   # ECP has no gate
     assert gated_call(lib, mode=3) == PI_ERR_UNSUPPORTED
@@ -170,8 +174,45 @@ def test_binding_fails_loudly_without_cuda():
     with pytest.raises((ValueError, RuntimeError)):
         pa.fwd(q, q, q, torch.ones(1, 2, 8), 4, 8, 1)
     with pytest.raises((ValueError, RuntimeError)):
-        pa.fwd_gated(q, q, q, torch.zeros(2, 64), torch.zeros(2), 4, 8, 1)
+        pa.fwd_gated(q, q, q, (torch.zeros(2, 8, 64), torch.zeros(2, 8), torch.zeros(2, 8), torch.zeros(2)), 4, 8, 1)
     with pytest.raises((ValueError, RuntimeError)):
         pa.decode(q[:, :, 0].contiguous(), q, q, torch.ones(1, 2), 4, 8, 1)
     with pytest.raises((ValueError, RuntimeError)):
         pa.bwd(q, q, q, torch.ones(1, 2, 8), q, torch.zeros(1, 2, 8), q, 4, 8, 1)
+
+
+@pytest.mark.parametrize("bad", ["dq", "dk", "dv", "dalpha"])
+@pytest.mark.parametrize("fn", ["bwd", "bwd_noalloc"])
+def test_backward_binding_checks_caller_gradient_buffers(monkeypatch, fn, bad):
+    """A caller-supplied gradient buffer is checked (device, dtype, shape, layout) before the
+    library is reached: the kernels store into it through maps sized from the inputs.  The CUDA
+    checks of the inputs are stubbed here (no GPU); the buffer named `bad` is a host tensor or
+    has the wrong shape, and the call must stop at it."""
+    import torch
+    from structured_sparse_long_gb300 import _binding
+
+    real = _binding._expect
+
+    def expect_without_device(t, name, dtype, shape=None):
+        if name != bad:
+            return
+        real(t, name, dtype, shape)  # the bad buffer: a host tensor -> "must be a CUDA tensor"
+
+    monkeypatch.setattr(_binding, "_expect", expect_without_device)
+    monkeypatch.setattr(_binding, "load", lambda: pytest.fail("the library was reached"))
+    monkeypatch.setattr(_binding, "bwd_workspace_size", lambda *a: 1024)
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    a = torch.ones(1, 2, 8)
+    grads = {"dq": q.clone(), "dk": q.clone(), "dv": q.clone(), "dalpha": torch.zeros(1, 2, 8)}
+    with pytest.raises(ValueError, match=bad):
+        getattr(_binding, fn)(q, q, q, a, q, torch.zeros(1, 2, 8), q, 4, 8, 1, **grads)
+
+    # the same buffer with the wrong shape is refused by the shape check as well
+    def expect_shape_only(t, name, dtype, shape=None):
+        if name == bad and shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+    monkeypatch.setattr(_binding, "_expect", expect_shape_only)
+    grads[bad] = grads[bad][..., :4].contiguous()  # last dimension cut: wrong shape
+    with pytest.raises(ValueError, match=bad):
+        getattr(_binding, fn)(q, q, q, a, q, torch.zeros(1, 2, 8), q, 4, 8, 1, **grads)

@@ -1,8 +1,8 @@
 """GPU parity of the fused gate (pi_attn_fwd_gated) against the fp64 oracle.
 
-The gate ("pi-Attention" page, section 2.3) is read as alpha = 1 / (1 + exp(-(q . w_h + c_h)))
-on the head's query; the kernel computes it from the Q tile it has staged and uses it exactly as
-pi_attn_fwd uses an alpha input.
+The gate ("pi-Attention" page, section 2.3: a light MLP per token and per head) is read as one
+hidden layer of 8 ReLU units on the head's query and a logistic output; the kernel computes it
+from the Q tile it has staged and uses it exactly as pi_attn_fwd uses an alpha input.
 """
 import numpy as np
 import pytest
@@ -38,13 +38,13 @@ def close(name, gpu, ref, tol):
 
 def run_case(w):
     inp = make_inputs(w, with_dout=False)
-    gw, gb = gate_weights(w.H, w.d, seed=w.seed + 100)
+    gate = gate_weights(w.H, w.d, seed=w.seed + 100)
     dev = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
-    out, lse, alpha = pa.fwd_gated(dev["q"], dev["k"], dev["v"], gw.cuda(), gb.cuda(), w.k_local,
+    out, lse, alpha = pa.fwd_gated(dev["q"], dev["k"], dev["v"], tuple(t.cuda() for t in gate), w.k_local,
                                    w.period, w.S, w.mode)
     torch.cuda.synchronize()
     assert pa.status() == 0
-    return inp, dev, gw, gb, out, lse, alpha
+    return inp, dev, gate, out, lse, alpha
 
 
 CASES = [
@@ -61,8 +61,9 @@ CASES = [
 def test_gated_forward_matches_oracle(spec):
     name, B, H, Hkv, N, d, k, per, S, mode = spec
     w = small_case(name, B, H, Hkv, N, d, k, per, S, mode, "bf16", seed=21)
-    inp, _, gw, gb, out, lse, alpha = run_case(w)
-    ref_out, ref_lse, ref_alpha = oracle.fwd_gated(inp["q"], inp["k"], inp["v"], gw, gb, k, per, S, mode)
+    inp, _, gate, out, lse, alpha = run_case(w)
+    ref_out, ref_lse, ref_alpha = oracle.fwd_gated(inp["q"], inp["k"], inp["v"], gate, k, per, S, mode)
+    assert 0.05 < float(np.std(ref_alpha)) and 0.0 < ref_alpha.min() and ref_alpha.max() < 1.0
     close("alpha", alpha.cpu().numpy(), ref_alpha, (1e-5, 1e-5))
     close("out", out.float().cpu().numpy(), ref_out, BF16)
     close("lse", lse.cpu().numpy(), ref_lse, BF16)
@@ -71,7 +72,7 @@ def test_gated_forward_matches_oracle(spec):
 def test_gated_forward_equals_forward_with_its_alpha():
     """The gate's alpha, fed to pi_attn_fwd, gives bit-identical out and lse."""
     w = small_case("g-eq", 1, 8, 2, 700, 128, 64, 96, 4, MODE_PI, "bf16", seed=22)
-    _, dev, _, _, out, lse, alpha = run_case(w)
+    _, dev, _, out, lse, alpha = run_case(w)
     out2, lse2 = pa.fwd(dev["q"], dev["k"], dev["v"], alpha, w.k_local, w.period, w.S, w.mode)
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
@@ -80,8 +81,8 @@ def test_gated_forward_equals_forward_with_its_alpha():
 def test_gated_c4_matches_oracle():
     """The long-context GQA layer (B1 H16 Hkv4 N65536 d128 k256 pi1024 S4) with the gate fused."""
     w = WORKLOADS["C4"]
-    inp, _, gw, gb, out, lse, alpha = run_case(w)
-    ref_out, ref_lse, ref_alpha = oracle.fwd_gated(inp["q"], inp["k"], inp["v"], gw, gb, w.k_local,
+    inp, _, gate, out, lse, alpha = run_case(w)
+    ref_out, ref_lse, ref_alpha = oracle.fwd_gated(inp["q"], inp["k"], inp["v"], gate, w.k_local,
                                                    w.period, w.S, w.mode)
     close("alpha", alpha.cpu().numpy(), ref_alpha, (1e-5, 1e-5))
     close("out", out.float().cpu().numpy(), ref_out, BF16)

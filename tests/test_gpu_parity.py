@@ -224,6 +224,37 @@ def test_alpha_edges():
     check_forward(ff, inp)
 
 
+def test_backward_alpha_edges():
+    """The backward where the gate saturates: alpha exactly 0 or 1 on some rows.  One prior is
+    then -inf; dalpha there is 0 (a saturated gate passes no gradient), finite everywhere, and
+    dq, dk, dv still match the oracle."""
+    for spec in (("bedges", 1, 2, 2, 260, 64, 20, 40, 3, MODE_PI, "bf16"),
+                 ("bedges128", 1, 4, 2, 200, 128, 30, 50, 2, MODE_PI, "bf16"),
+                 ("bedges32", 1, 2, 2, 130, 64, 20, 40, 3, MODE_PI, "f32")):
+        w = small(spec).replace(backward=True)
+        inp = make_inputs(w, with_dout=True)
+        a = inp["alpha"].clone()
+        a[:, 0, ::3] = 0.0
+        a[:, -1, 1::4] = 1.0
+        inp["alpha"] = a
+        _, dev, out, lse = run_forward(w, inp)
+        dq, dk, dv, dal = pa.bwd(dev["q"], dev["k"], dev["v"], dev["alpha"], out, lse, dev["dout"],
+                                 w.k_local, w.period, w.S, w.mode)
+        torch.cuda.synchronize()
+        assert pa.status() == 0
+        dal = dal.cpu()
+        assert torch.isfinite(dal).all(), "non-finite dalpha"
+        sat = (a == 0.0) | (a == 1.0)
+        assert torch.count_nonzero(dal[sat]) == 0, "dalpha must be 0 where the gate saturates"
+        rq, rk, rv, ral = oracle.bwd(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["dout"], w.k_local,
+                                     w.period, w.S, w.mode)
+        assert np.all(ral[sat.numpy()] == 0.0)
+        assert_close(f"{w.name} dq", dq.float().cpu().numpy(), rq, w.dtype)
+        assert_close(f"{w.name} dk", dk.float().cpu().numpy(), rk, w.dtype)
+        assert_close(f"{w.name} dv", dv.float().cpu().numpy(), rv, w.dtype)
+        assert_close(f"{w.name} dalpha", dal.numpy(), ral, w.dtype)
+
+
 def test_forward_is_deterministic():
     w = WORKLOADS["C2"]
     inp, dev, out1, lse1 = run_forward(w)

@@ -408,3 +408,38 @@ def test_dalpha_skip_only_form_and_zero_without_skips():
     np.testing.assert_allclose(dal, ref.numpy(), atol=1e-9, rtol=1e-9)
     _, _, _, dal0 = oracle.bwd(q, k, v, a, dout, kl, per, 0, 0)
     np.testing.assert_allclose(dal0, 0.0, atol=1e-12)
+
+
+def test_dalpha_at_a_saturated_gate_is_zero_and_the_rest_unchanged():
+    """At alpha exactly 0 or 1 one prior is -inf and its weights are exactly 0; the oracle takes
+    dalpha there as 0 (a saturated gate passes no gradient) instead of 0/0.  Every other row keeps
+    the chain-rule value, and dq, dk, dv still match autograd through the dense form."""
+    B, H, N, d, kl, per, S = 1, 2, 40, 5, 4, 9, 3
+    q, k, v, a = rand_case(B, H, H, N, d, seed=78, alpha_lo=0.2, alpha_hi=0.8)
+    g = torch.Generator().manual_seed(4)
+    dout = torch.randn(B, H, N, d, generator=g, dtype=torch.float64)
+    a_sat = a.clone()
+    a_sat[:, 0, ::3] = 0.0
+    a_sat[:, 1, 1::4] = 1.0
+    sat = ((a_sat == 0.0) | (a_sat == 1.0)).numpy()
+    dq, dk, dv, dal = oracle.bwd(q, k, v, a_sat, dout, kl, per, S, 0)
+    assert np.all(np.isfinite(dal)) and np.all(dal[sat] == 0.0)
+    _, _, _, dal_ref = oracle.bwd(q, k, v, a, dout, kl, per, S, 0)
+    # rows whose gate did not change keep their value (each row's dalpha depends on that row only)
+    unchanged = (a_sat == a).numpy()
+    np.testing.assert_allclose(dal[unchanged], dal_ref[unchanged], rtol=1e-12, atol=0)
+    # dense reference with the union masks; rows with alpha = 0 and no skip key have no finite
+    # logit: their output is 0 and they pass no gradient
+    qt, kt, vt = (t.clone().requires_grad_(True) for t in (q, k, v))
+    local, skip = union_masks(N, kl, per, S, 0)
+    ad = a_sat.double().unsqueeze(-1)
+    scores = (qt @ kt.transpose(-1, -2)) / math.sqrt(d)
+    ninf = torch.tensor(-math.inf, dtype=torch.float64)
+    z = torch.where(local, scores + torch.log(ad), torch.where(skip, scores + torch.log1p(-ad), ninf))
+    dead = torch.isinf(z).all(-1, keepdim=True)
+    p_ = torch.softmax(torch.where(dead, torch.zeros_like(z), z), -1)
+    out = (p_ @ vt) * (~dead)
+    out.backward(dout)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-10, rtol=0)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-10, rtol=0)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-10, rtol=0)

@@ -68,6 +68,9 @@ def test_noalloc_backward_matches_workspace_backward_on_consecutive_calls():
         assert pa.status() == 0
         for name, a, b in zip(("dq", "dk", "dv", "dalpha"), got, ref):
             _close(f"{w.name} {name}", a, b)
+            # the same deterministic kernels on the same inputs: identical bits, so that a row
+            # of the shared scratch left over from the previous call would show
+            assert torch.equal(a, b), f"{w.name} {name}: differs from the workspace backward"
 
 
 def test_noalloc_rejects_sizes_above_its_scratch():
