@@ -178,6 +178,48 @@ int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *al
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pi_attn_fwd_shard -- pi_attn_fwd for one shard of a sequence split over
+ * devices (the "pi-Attention" page, section 2, item 2: the periodic skips suit
+ * collective communication; its efficiency results are on 8 GPUs).  A shard owns
+ * the queries at global positions [t0, t0 + Nq); it holds, in local buffers, the
+ * key/value rows of a window [w0, w0 + Nkv) of the sequence that contains every
+ * key those queries attend (its own rows and a halo received from other shards;
+ * window rows that no query attends may hold anything finite, e.g. zeros).
+ * q_offset = t0 - w0 is the key row of the shard's first query.
+ *   q, out [B,H,Nq,d] and alpha, lse [B,H,Nq] (the shard's queries); k, v
+ *   [B,Hkv,Nkv,d] (the window).  Row r of q is the query at key row q_offset + r;
+ *   inside the window every rule of pi_attn_fwd holds with positions taken
+ *   relative to w0, so the window must start where the neighbour sets do not
+ *   change under the shift: w0 = 0, or every key of every shard query inside the
+ *   window (the skips i - m*period and the band), and in ECP mode w0 a multiple
+ *   of c = k_local.  The result is then identical to rows [t0, t0 + Nq) of
+ *   pi_attn_fwd over the whole sequence.
+ *   Requirements: 0 <= q_offset, q_offset + Nq <= Nkv, q_offset a multiple of
+ *   128 (else PI_ERR_SHAPE).  bf16; other arguments, errors and rules as
+ *   pi_attn_fwd (N there is Nkv here).
+ */
+int pi_attn_fwd_shard(const void *q, const void *k, const void *v, const float *alpha,
+                      int B, int H, int Hkv, int Nq, int Nkv, int q_offset, int d, int k_local,
+                      int period, int S, int mode, void *out, float *lse, void *stream);
+
+/*
+ * pi_attn_bwd_shard -- pi_attn_bwd for the shard of pi_attn_fwd_shard.
+ *   q, out, dout, dq [B,H,Nq,d], alpha, lse, dalpha [B,H,Nq] (the shard's
+ *   queries); k, v, dk, dv [B,Hkv,Nkv,d] (the window).  dq and dalpha are the
+ *   shard's rows of the whole-sequence gradients.  dk and dv are this shard's
+ *   queries' part of the gradients of the window's rows: the whole-sequence dk
+ *   and dv of a key row are the sum of these parts over every shard whose window
+ *   holds it (the halo rows' parts go back to the shards that own them).
+ *   workspace: at least pi_attn_bwd_workspace_size(B, H, Hkv, Nq, d) bytes.
+ *   Window requirements as pi_attn_fwd_shard; other rules as pi_attn_bwd.
+ */
+int pi_attn_bwd_shard(const void *q, const void *k, const void *v, const float *alpha,
+                      const void *out, const float *lse, const void *dout,
+                      int B, int H, int Hkv, int Nq, int Nkv, int q_offset, int d, int k_local,
+                      int period, int S, int mode, void *dq, void *dk, void *dv, float *dalpha,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pi_attn_bwd_noalloc -- the bf16 backward of pi_attn_bwd, for callers that
  * cannot hand the library a workspace and must not allocate device memory
  * themselves.  The paper has no counterpart to this entry point; it exists
@@ -202,6 +244,10 @@ int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *al
  *     reads.  Calls whose kernels overlap on the GPU (different streams
  *     without ordering between them) race on the array and give undefined
  *     results; order them on one stream or with events.
+ *   - The cached address belongs to the device's current context: after
+ *     cudaDeviceReset on a device, make no further call of this library on it
+ *     in the same process (the same holds for the status word of every entry
+ *     point).
  */
 #define PI_ATTN_NOALLOC_MAX_ROWS (1 << 20)
 int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float *alpha,

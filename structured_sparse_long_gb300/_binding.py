@@ -20,7 +20,7 @@ from . import build as _build
 
 MODE_PI = 0
 MODE_ECP = 1
-MODE_PI_BIDIR = 2  # bidirectional band and skips (forward only)
+MODE_PI_BIDIR = 2  # bidirectional band and skips
 PI_OK = 0
 
 _lock = threading.Lock()
@@ -71,6 +71,10 @@ def load() -> ctypes.CDLL:
         lib.pi_attn_decode.restype = I
         lib.pi_attn_fwd_gated.argtypes = [P, P, P, P, P, P, P] + [I] * 9 + [P, P, P, P]
         lib.pi_attn_fwd_gated.restype = I
+        lib.pi_attn_fwd_shard.argtypes = [P, P, P, P] + [I] * 11 + [P, P, P]
+        lib.pi_attn_fwd_shard.restype = I
+        lib.pi_attn_bwd_shard.argtypes = [P, P, P, P, P, P, P] + [I] * 11 + [P, P, P, P, P, Z, P]
+        lib.pi_attn_bwd_shard.restype = I
         for name in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
                      "pi_attn_status", "pi_attn_debug_counts", "pi_attn_debug_probs",
                      "pi_attn_debug_wait_timeout"):
@@ -275,6 +279,64 @@ def bwd_noalloc(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: in
                                     _ptr(dout), B, H, Hkv, N, d, k_local, period, S, mode,
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _stream(stream))
     _check("pi_attn_bwd_noalloc", rc)
+    return dq, dk, dv, dalpha
+
+
+def _shard_sizes(q, k):
+    if q.dim() != 4 or k.dim() != 4 or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B,H,Nq,d] and k [B,Hkv,Nkv,d]")
+    B, H, Nq, d = q.shape
+    return B, H, k.shape[1], Nq, k.shape[2], d
+
+
+def fwd_shard(q, k, v, alpha, q_offset: int, k_local: int, period: int, S: int, mode: int = MODE_PI,
+              out=None, lse=None, stream=None):
+    """pi_attn_fwd_shard (bf16): the queries q [B,H,Nq,d] of a sequence shard, the first at key
+    row q_offset of the local key/value window k, v [B,Hkv,Nkv,d].  Returns (out, lse)."""
+    B, H, Hkv, Nq, Nkv, d = _shard_sizes(q, k)
+    _expect(q, "q", torch.bfloat16)
+    _expect(k, "k", torch.bfloat16)
+    _expect(v, "v", torch.bfloat16, k.shape)
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H, Nq))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    _expect_like(out, "out", q, torch.bfloat16, q.shape)
+    _expect_like(lse, "lse", q, torch.float32, (B, H, Nq))
+    rc = load().pi_attn_fwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, Nq, Nkv,
+                                  int(q_offset), d, k_local, period, S, mode, _ptr(out), _ptr(lse),
+                                  _stream(stream))
+    _check("pi_attn_fwd_shard", rc)
+    return out, lse
+
+
+def bwd_shard(q, k, v, alpha, out, lse, dout, q_offset: int, k_local: int, period: int, S: int,
+              mode: int = MODE_PI, dq=None, dk=None, dv=None, dalpha=None, workspace=None,
+              stream=None):
+    """pi_attn_bwd_shard (bf16).  Returns (dq, dk, dv, dalpha): dq and dalpha of the shard's
+    queries, dk and dv [B,Hkv,Nkv,d] the shard's part of the window rows' gradients."""
+    B, H, Hkv, Nq, Nkv, d = _shard_sizes(q, k)
+    for t, n in ((q, "q"), (out, "out"), (dout, "dout")):
+        _expect(t, n, torch.bfloat16, q.shape)
+    for t, n in ((k, "k"), (v, "v")):
+        _expect(t, n, torch.bfloat16, k.shape)
+    _expect(lse, "lse", torch.float32, (B, H, Nq))
+    if alpha is not None:
+        _expect(alpha, "alpha", torch.float32, (B, H, Nq))
+    dq, dk, dv, dalpha = _grad_buffers(q, k, v, dq, dk, dv, dalpha)
+    nbytes = bwd_workspace_size(B, H, Hkv, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+    _expect_like(workspace, "workspace", q, torch.uint8, None)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace must hold {nbytes} bytes, got {workspace.numel()}")
+    rc = load().pi_attn_bwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse),
+                                  _ptr(dout), B, H, Hkv, Nq, Nkv, int(q_offset), d, k_local, period,
+                                  S, mode, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
+                                  _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("pi_attn_bwd_shard", rc)
     return dq, dk, dv, dalpha
 
 

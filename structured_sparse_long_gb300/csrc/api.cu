@@ -62,11 +62,29 @@ int validate_fwd(const void *q, const void *k, const void *v, const float *alpha
     return PI_OK;
 }
 
-pi::Shape make_shape(int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode) {
+// Query rows of a sequence shard's call: nq rows whose first is the query at key position
+// qoff.  A whole-sequence call has none (shard = false: the queries are the N key rows).
+struct Window {
+    bool shard;
+    int nq, qoff;
+};
+
+// A sequence shard's window: inside the key rows, starting on a 128-row boundary, so that the
+// kernels see the same query blocks as in a whole-sequence run over the key rows.
+int validate_window(int N, Window w) {
+    if (w.nq <= 0 || w.qoff < 0 || (long long)w.qoff + w.nq > (long long)N) return PI_ERR_SHAPE;
+    if (w.qoff % 128 != 0) return PI_ERR_SHAPE;
+    return PI_OK;
+}
+
+pi::Shape make_shape(int B, int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
+                     Window w = Window{false, 0, 0}) {
     pi::Shape s;
     s.B = B; s.H = H; s.Hkv = Hkv; s.N = N; s.d = d;
     s.k_local = k_local; s.period = period; s.S = (mode != PI_MODE_ECP) ? S : 0; s.mode = mode;
     s.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
+    s.nq = w.shard ? w.nq : N;
+    s.qoff = w.shard ? w.qoff : 0;
     return s;
 }
 
@@ -74,15 +92,17 @@ int map_cuda(cudaError_t e) { return e == cudaSuccess ? PI_OK : PI_ERR_CUDA; }
 
 int run_fwd(const void *q, const void *k, const void *v, const float *alpha, int B, int H, int Hkv,
             int N, int d, int k_local, int period, int S, int mode, void *out, float *lse, void *stream,
-            bool fp32, int dbg, int *cnt, long long *isum, const float *lse_in, float *P) {
-    const int rc = validate_fwd(q, k, v, alpha, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
+            bool fp32, int dbg, int *cnt, long long *isum, const float *lse_in, float *P,
+            Window w = Window{false, 0, 0}) {
+    int rc = validate_fwd(q, k, v, alpha, B, H, Hkv, N, d, k_local, period, S, mode, out, lse);
     if (rc != PI_OK) return rc;
+    if (w.shard && (rc = validate_window(N, w)) != PI_OK) return rc;
     int *status = status_word();
     if (!status) return PI_ERR_CUDA;
     pi::LaunchFwd L;
     L.q = q; L.k = k; L.v = v; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
     L.out = out; L.lse = lse;
-    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode, w);
     L.fp32 = fp32; L.dbg = dbg; L.cnt = cnt; L.isum = isum; L.lse_in = lse_in; L.P = P;
     L.trace = nullptr; L.n_trace = 0;
     L.status = status; L.timeout_ns = kWaitTimeoutNs;
@@ -94,24 +114,25 @@ int run_fwd(const void *q, const void *k, const void *v, const float *alpha, int
 int run_bwd(const void *q, const void *k, const void *v, const float *alpha, const void *out,
             const float *lse, const void *dout, int B, int H, int Hkv, int N, int d, int k_local,
             int period, int S, int mode, void *dq, void *dk, void *dv, float *dalpha, void *workspace,
-            size_t workspace_bytes, void *stream, bool fp32) {
+            size_t workspace_bytes, void *stream, bool fp32, Window w = Window{false, 0, 0}) {
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return PI_ERR_NULL;
     if (mode != PI_MODE_ECP && !alpha) return PI_ERR_NULL;
-    const int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    int rc = validate_shape(B, H, Hkv, N, d, k_local, period, S, mode);
     if (rc != PI_OK) return rc;
+    if (w.shard && (rc = validate_window(N, w)) != PI_OK) return rc;
     const void *p16[] = {q, k, v, out, dout, dq, dk, dv};
     for (const void *p : p16)
         if (!aligned(p, 16)) return PI_ERR_ALIGN;
     if (!aligned(lse, 4) || (alpha && !aligned(alpha, 4)) || (dalpha && !aligned(dalpha, 4)))
         return PI_ERR_ALIGN;
-    const size_t need = pi_attn_bwd_workspace_size(B, H, Hkv, N, d);
+    const size_t need = pi_attn_bwd_workspace_size(B, H, Hkv, w.shard ? w.nq : N, d);
     if (!workspace || workspace_bytes < need) return PI_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PI_ERR_ALIGN;
     pi::LaunchBwd L;
     L.q = q; L.k = k; L.v = v; L.alpha = (mode != PI_MODE_ECP) ? alpha : nullptr;
     L.out = out; L.lse = lse; L.dout = dout; L.dq = dq; L.dk = dk; L.dv = dv; L.dalpha = dalpha;
     L.Dws = static_cast<float *>(workspace);
-    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode);
+    L.s = make_shape(B, H, Hkv, N, d, k_local, period, S, mode, w);
     L.fp32 = fp32;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!fp32 && d != 32) {
@@ -214,6 +235,21 @@ int pi_attn_bwd_f32(const void *q, const void *k, const void *v, const float *al
                     float *dalpha, void *workspace, size_t workspace_bytes, void *stream) {
     return run_bwd(q, k, v, alpha, out, lse, dout, B, H, Hkv, N, d, k_local, period, S, mode, dq, dk,
                    dv, dalpha, workspace, workspace_bytes, stream, true);
+}
+
+int pi_attn_fwd_shard(const void *q, const void *k, const void *v, const float *alpha, int B, int H,
+                      int Hkv, int Nq, int Nkv, int q_offset, int d, int k_local, int period, int S,
+                      int mode, void *out, float *lse, void *stream) {
+    return run_fwd(q, k, v, alpha, B, H, Hkv, Nkv, d, k_local, period, S, mode, out, lse, stream, false,
+                   0, nullptr, nullptr, nullptr, nullptr, Window{true, Nq, q_offset});
+}
+
+int pi_attn_bwd_shard(const void *q, const void *k, const void *v, const float *alpha, const void *out,
+                      const float *lse, const void *dout, int B, int H, int Hkv, int Nq, int Nkv,
+                      int q_offset, int d, int k_local, int period, int S, int mode, void *dq, void *dk,
+                      void *dv, float *dalpha, void *workspace, size_t workspace_bytes, void *stream) {
+    return run_bwd(q, k, v, alpha, out, lse, dout, B, H, Hkv, Nkv, d, k_local, period, S, mode, dq, dk,
+                   dv, dalpha, workspace, workspace_bytes, stream, false, Window{true, Nq, q_offset});
 }
 
 int pi_attn_bwd_noalloc(const void *q, const void *k, const void *v, const float *alpha,

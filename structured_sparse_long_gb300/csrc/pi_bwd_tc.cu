@@ -150,7 +150,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // ---- q-block coordinates and key chunks (as in the forward)
     const int GP = args.GP;
     const int R = BM / GP;
-    const int nqb = (s.N + R - 1) / R;
+    const int nqb = (s.nq + R - 1) / R;
     const int hsub = s.H / GP;
     int bid = blockIdx.x;
     const int pb = bid % nqb;
@@ -159,7 +159,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int b = bid / hsub;
     const int h0 = hs * GP;
     const int g = h0 / (s.H / s.Hkv);
-    const int p0 = pb * R;
+    const int p0 = s.qoff + pb * R;  // key position of the block's first query row
     QWalk cw;
     cw.p0 = p0;
     cw.period = s.period;
@@ -206,8 +206,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const uint64_t once = policy_evict_first(), reused = policy_evict_last();
             mbar_expect_tx(bar(C::B_QF), 2 * C::Q_BYTES);
             for (int dc = 0; dc < C::KD; ++dc) {
-                tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0, b * s.H + h0, bar(C::B_QF), once);
-                tma_load_3d_hint(sG + dc * C::Q_DBLK, &tmG, dc * 64, p0, b * s.H + h0, bar(C::B_QF), once);
+                tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, p0 - s.qoff, b * s.H + h0, bar(C::B_QF), once);
+                tma_load_3d_hint(sG + dc * C::Q_DBLK, &tmG, dc * 64, p0 - s.qoff, b * s.H + h0, bar(C::B_QF), once);
             }
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
@@ -337,8 +337,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int hh = r / R, trow = r % R;
         const int i = p0 + trow;
         const int h = h0 + hh;
-        const bool row_ok = i < s.N;
-        const long long row_g = ((long long)b * s.H + h) * s.N + i;
+        const bool row_ok = i - s.qoff < s.nq;
+        const long long row_g = ((long long)b * s.H + h) * s.nq + (i - s.qoff);
         const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
         const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
         const float off_skip = log2f(1.f - al);
@@ -470,7 +470,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (ok && warp == 4 && lane == 0) {
             const uint64_t once = policy_evict_first();
             for (int dc = 0; dc < C::KD; ++dc)
-                tma_store_3d(&tmDQ, sQ + dc * C::Q_DBLK, dc * 64, p0, b * s.H + h0, once);
+                tma_store_3d(&tmDQ, sQ + dc * C::Q_DBLK, dc * 64, p0 - s.qoff, b * s.H + h0, once);
             tma_store_commit_and_wait();
         }
         if (ok && row_ok) {
@@ -683,10 +683,10 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 const int plane = b * s.H + g * G + hh;
                 mbar_expect_tx(bar(C::B_QF + st), 2 * C::QC_BYTES);
                 for (int dc = 0; dc < C::KD; ++dc) {
-                    tma_load_3d_hint(sQ + st * C::QC_BYTES + dc * C::QC_DBLK, &tmQc, dc * 64, i0, plane,
-                                     bar(C::B_QF + st), reused);
-                    tma_load_3d_hint(sG + st * C::QC_BYTES + dc * C::QC_DBLK, &tmGc, dc * 64, i0, plane,
-                                     bar(C::B_QF + st), reused);
+                    tma_load_3d_hint(sQ + st * C::QC_BYTES + dc * C::QC_DBLK, &tmQc, dc * 64, i0 - s.qoff,
+                                     plane, bar(C::B_QF + st), reused);
+                    tma_load_3d_hint(sG + st * C::QC_BYTES + dc * C::QC_DBLK, &tmGc, dc * 64, i0 - s.qoff,
+                                     plane, bar(C::B_QF + st), reused);
                 }
                 issued = ci + 1;
             }
@@ -711,18 +711,20 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             int hh, i0, back;
             bool sk;
             kw.chunk(ci, hh, i0, back, sk);
-            const long long rbase = ((long long)b * s.H + g * G + hh) * s.N;
+            const long long rbase = ((long long)b * s.H + g * G + hh) * s.nq;
             float *xb = xvec + st * 2 * QC;
 #pragma unroll
             for (int e = 0; e < QC / 32; ++e) {
-                const int c = lane + 32 * e, i = i0 + c;
+                const int c = lane + 32 * e, iq = i0 + c - s.qoff;  // row of the query window
                 float bias = -INFINITY, dv = 0.f;
-                if (i >= 0 && i < s.N) {  // skip chunks of the bidirectional mode may start before 0
-                    const float lse2 = args.lse[rbase + i] * kLog2e;
-                    const float al = args.alpha ? args.alpha[rbase + i] : 1.f;
+                // skip chunks of the bidirectional mode may start before 0; positions outside the
+                // query window (a sequence shard's halo) have no query and take P = 0
+                if (iq >= 0 && iq < s.nq) {
+                    const float lse2 = args.lse[rbase + iq] * kLog2e;
+                    const float al = args.alpha ? args.alpha[rbase + iq] : 1.f;
                     const float prior = (s.mode == kModeEcp) ? 0.f : (sk ? log2f(1.f - al) : log2f(al));
                     if (lse2 != -INFINITY) bias = prior - lse2;
-                    dv = args.Dws[rbase + i];
+                    dv = args.Dws[rbase + iq];
                 }
                 xb[c] = bias;
                 xb[QC + c] = dv;
@@ -940,15 +942,15 @@ cudaError_t launch_bwd_dq_tc(const LaunchBwd &L, int *status, uint64_t timeout_n
     const int GP = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
     const int R = BM / GP;
     CUtensorMap mq, mg, mk, mv, mdq;
-    if (!make_map(&mq, L.q, s.d, s.N, (long long)s.B * s.H, R, GP) ||
-        !make_map(&mg, L.dout, s.d, s.N, (long long)s.B * s.H, R, GP) ||
-        !make_map(&mdq, L.dq, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+    if (!make_map(&mq, L.q, s.d, s.nq, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mg, L.dout, s.d, s.nq, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mdq, L.dq, s.d, s.nq, (long long)s.B * s.H, R, GP) ||
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
     DqArgs a{static_cast<const __nv_bfloat16 *>(L.out), static_cast<const __nv_bfloat16 *>(L.dout), L.alpha,
              L.lse, L.Dws, L.dalpha, s, GP, status, timeout_ns};
-    const long long grid = (long long)s.B * (s.H / GP) * ((s.N + R - 1) / R);
+    const long long grid = (long long)s.B * (s.H / GP) * ((s.nq + R - 1) / R);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (s.d == 64) return launch_dq<64>(mq, mg, mk, mv, mdq, a, (unsigned)grid, st);
     if (s.d == 128) return launch_dq<128>(mq, mg, mk, mv, mdq, a, (unsigned)grid, st);
@@ -963,8 +965,8 @@ cudaError_t launch_bwd_dkdv_tc(const LaunchBwd &L, int *status, uint64_t timeout
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
         !make_map(&mdk, L.dk, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
         !make_map(&mdv, L.dv, s.d, s.N, (long long)s.B * s.Hkv, BK, 1) ||
-        !make_map(&mqc, L.q, s.d, s.N, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1) ||
-        !make_map(&mgc, L.dout, s.d, s.N, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1))
+        !make_map(&mqc, L.q, s.d, s.nq, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1) ||
+        !make_map(&mgc, L.dout, s.d, s.nq, (long long)s.B * s.H, s.d == 64 ? CfgK<64>::QC : CfgK<128>::QC, 1))
         return cudaErrorNotSupported;
     DkvArgs a{L.alpha, L.lse, L.Dws, s, status, timeout_ns};
     const long long grid = (long long)s.B * s.Hkv * ((s.N + BK - 1) / BK);

@@ -33,6 +33,11 @@ struct Shape {
     int S;             // skip multiples (pi mode)
     int mode;          // 0 = pi (causal), 1 = ECP, 2 = pi (bidirectional)
     float scale_log2;  // log2(e) / sqrt(d): raw score -> log2-domain logit
+    // Query rows.  Row r of a (b, h) plane of q, out, lse, alpha (and of their gradients) is
+    // the query at key position qoff + r, for r < nq; N counts the key/value rows.  A whole
+    // sequence has nq = N and qoff = 0; a sequence shard has its queries [t0, t1) against a
+    // local key window that starts qoff = t0 - (window start) rows before them.
+    int nq, qoff;
 };
 
 constexpr int kModeEcp = 1;

@@ -292,7 +292,7 @@ __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc
     d.h0 = (rest - b * a.ngrp) * a.GP;
     d.b = b;
     d.g = a.div_G.div(d.h0);
-    d.p0 = pb * R;
+    d.p0 = s.qoff + pb * R;  // key position of the block's first query row
     ChunkWalk &cw = d.cw;
     cw.p0 = d.p0;
     cw.period = s.period;
@@ -438,7 +438,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     auto issue_q = [&](const BlockDesc &bd) {
         mbar_expect_tx(bar(C::B_Q), C::Q_BYTES);
         for (int dc = 0; dc < C::KD; ++dc)
-            tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, bd.p0, bd.b * s.H + bd.h0, bar(C::B_Q),
+            tma_load_3d_hint(sQ + dc * C::Q_DBLK, &tmQ, dc * 64, bd.p0 - s.qoff, bd.b * s.H + bd.h0, bar(C::B_Q),
                              policy_evict_first());
     };
 
@@ -531,7 +531,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             auto store_out = [&](const BlockDesc &bd, int kb) -> bool {
                 if (!wait_bar(bar(C::B_STF), (uint32_t)(kb & 1), wc)) return false;
                 for (int dc = 0; dc < C::KD; ++dc)
-                    tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, bd.p0, bd.b * s.H + bd.h0, stream_once);
+                    tma_store_3d(&tmO, sQ + dc * C::Q_DBLK, dc * 64, bd.p0 - s.qoff, bd.b * s.H + bd.h0,
+                                 stream_once);
                 tma_store_commit_and_wait();
                 mbar_arrive(bar(C::B_STR));
                 return true;
@@ -689,9 +690,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // input's is loaded after the out-of-line copy (a load in flight across a call would
         // be waited for there); it was prefetched into L2 a block ahead.
         auto copy_q = [&](const BlockDesc &bd, int kb, float &al_out) -> bool {
-            const int i = bd.p0 + trow, h = bd.h0 + hh;
-            const bool row_ok = i < s.N;
-            const long long row_g = ((long long)bd.b * s.H + h) * s.N + i;
+            const int iq = bd.p0 - s.qoff + trow, h = bd.h0 + hh;
+            const bool row_ok = iq < s.nq;
+            const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), (uint32_t)(kb & 1), wc))) return false;
             constexpr bool gated = GATE;
             const float z = copy_q_row<D, GATE>(
@@ -719,9 +720,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             BlockDesc bd;
             describe_block(L, args, bd);
             const bool has_next = L < args.n_blocks - LS;
-            const int i = bd.p0 + trow, h = bd.h0 + hh;
-            const bool row_ok = i < s.N;
-            const long long row_g = ((long long)bd.b * s.H + h) * s.N + i;
+            const int i = bd.p0 + trow, h = bd.h0 + hh, iq = i - s.qoff;
+            const bool row_ok = iq < s.nq;
+            const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
             const float al = al_next;
             const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
             const float off_skip = log2f(1.f - al);
@@ -737,8 +738,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int rest = args.div_nqb.div(Ln);
                 const int bn = args.div_ngrp.div(rest);
                 const int in = (Ln - rest * args.nqb) * R + trow;
-                if (in < s.N)
-                    prefetch_l2(args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.N + in);
+                if (in < s.nq)
+                    prefetch_l2(args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.nq + in);
             }
 
             for (int t = 0; t < bd.n_tiles; ++t, ++gsm) {
@@ -988,13 +989,13 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     const int GP = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
     const int R = BM / GP;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, L.q, s.d, s.N, (long long)s.B * s.H, R, GP) ||
-        !make_map(&mo, L.out, s.d, s.N, (long long)s.B * s.H, R, GP) ||
+    if (!make_map(&mq, L.q, s.d, s.nq, (long long)s.B * s.H, R, GP) ||
+        !make_map(&mo, L.out, s.d, s.nq, (long long)s.B * s.H, R, GP) ||
         !make_map(&mk, L.k, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1) ||
         !make_map(&mv, L.v, s.d, s.N, (long long)s.B * s.Hkv, CHUNK, 1))
         return cudaErrorNotSupported;
     const int m_first = (s.mode != kModeEcp && s.S > 0) ? first_skip_multiple(s) : 1;
-    const int nqb = (s.N + R - 1) / R, ngrp = s.H / GP;
+    const int nqb = (s.nq + R - 1) / R, ngrp = s.H / GP;
     const long long nb64 = (long long)nqb * ngrp * s.B;
     if (nb64 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int n_blocks = (int)nb64;

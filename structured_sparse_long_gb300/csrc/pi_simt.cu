@@ -72,11 +72,11 @@ template <typename T, int D, int DBG>
 __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(FwdArgs a, Shape s) {
     __shared__ __align__(16) float qs[kWarps][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long rows = (long long)s.B * s.H * s.N;
+    const long long rows = (long long)s.B * s.H * s.nq;
     const long long row = (long long)blockIdx.x * kWarps + warp;
     if (row >= rows) return;  // uniform per warp
-    const int i = (int)(row % s.N);
-    const long long bh = row / s.N;
+    const int i = s.qoff + (int)(row % s.nq);  // key position of the query
+    const long long bh = row / s.nq;
     const int h = (int)(bh % s.H), b = (int)(bh / s.H);
     const int g = h / (s.H / s.Hkv);
     const T *qrow = static_cast<const T *>(a.q) + row * D;
@@ -178,11 +178,11 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_kernel(BwdArgs a, Shape s)
     __shared__ __align__(16) float qs[kWarps][D];
     __shared__ __align__(16) float gs[kWarps][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long rows = (long long)s.B * s.H * s.N;
+    const long long rows = (long long)s.B * s.H * s.nq;
     const long long row = (long long)blockIdx.x * kWarps + warp;
     if (row >= rows) return;
-    const int i = (int)(row % s.N);
-    const long long bh = row / s.N;
+    const int i = s.qoff + (int)(row % s.nq);  // key position of the query
+    const long long bh = row / s.nq;
     const int h = (int)(bh % s.H), b = (int)(bh / s.H);
     const int g = h / (s.H / s.Hkv);
     const T *qrow = static_cast<const T *>(a.q) + row * D;
@@ -292,21 +292,24 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
 
     for (int hh = 0; hh < G; ++hh) {
         const int h = g * G + hh;
-        const long long rbase = ((long long)b * s.H + h) * s.N;  // query row index base
+        // the query at key position i is row i - qoff of the plane; only positions inside the
+        // query window [wlo, whi] are visited
+        const long long rbase = ((long long)b * s.H + h) * s.nq;
         const T *qb = static_cast<const T *>(a.q) + rbase * D;
         const T *gb = static_cast<const T *>(a.dout) + rbase * D;
+        const int wlo = s.qoff, whi = s.qoff + s.nq - 1;
 
         auto chunk = [&](int i, bool valid, bool is_skip) {
             float p = 0.f, dz = 0.f;
             if (valid) {
-                const long long row = rbase + i;
+                const long long row = rbase + (i - s.qoff);
                 const float lse2 = a.lse[row] * kLog2e;
                 if (lse2 != -INFINITY) {
                     const float al = a.alpha ? a.alpha[row] : 1.f;
                     const float off = (s.mode != kModeEcp) ? (is_skip ? log2f(1.f - al) : log2f(al)) : 0.f;
-                    const float z = fmaf(dot_row<T, D>(ks[warp], qb + (long long)i * D), s.scale_log2, off);
+                    const float z = fmaf(dot_row<T, D>(ks[warp], qb + (long long)(i - s.qoff) * D), s.scale_log2, off);
                     p = exp2f(z - lse2);
-                    const float dp = dot_row<T, D>(vs[warp], gb + (long long)i * D);
+                    const float dp = dot_row<T, D>(vs[warp], gb + (long long)(i - s.qoff) * D);
                     dz = p * (dp - a.Dws[row]);
                 }
             }
@@ -315,8 +318,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
                 const float dzc = __shfl_sync(kFull, dz, c);
                 const int ic = __shfl_sync(kFull, i, c);
                 if (pc != 0.f || dzc != 0.f) {
-                    const T *qr = qb + (long long)ic * D;
-                    const T *gr = gb + (long long)ic * D;
+                    const T *qr = qb + (long long)(ic - s.qoff) * D;
+                    const T *gr = gb + (long long)(ic - s.qoff) * D;
 #pragma unroll
                     for (int r = 0; r < RC; ++r) {
                         dv[r] = fmaf(pc, to_f32(gr[lane + 32 * r]), dv[r]);
@@ -326,8 +329,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
             }
         };
 
-        const int ifirst = band_first_query(j, s.mode, s.k_local);
-        const int ilast = band_last_query(j, s.N, s.mode, s.k_local);
+        const int ifirst = max(band_first_query(j, s.mode, s.k_local), wlo);
+        const int ilast = min(band_last_query(j, s.N, s.mode, s.k_local), whi);
         for (int i0 = ifirst; i0 <= ilast; i0 += 32) {
             const int i = i0 + lane;
             chunk(i, i <= ilast, false);
@@ -339,8 +342,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
                     const int mm = m0 + lane;
                     const long long back = (long long)mm * s.period;
                     const long long ii = (long long)j + dir * back;
-                    const bool valid = mm <= s.S && back > s.k_local && ii >= 0 && ii < s.N;
-                    chunk(valid ? (int)ii : 0, valid, true);
+                    const bool valid = mm <= s.S && back > s.k_local && ii >= wlo && ii <= whi;
+                    chunk(valid ? (int)ii : wlo, valid, true);
                 }
             }
         }
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_kernel(BwdArgs a, Shape 
 
 template <typename T, int D>
 static cudaError_t fwd_dispatch_dbg(const FwdArgs &a, const Shape &s, int dbg, cudaStream_t st) {
-    const long long rows = (long long)s.B * s.H * s.N;
+    const long long rows = (long long)s.B * s.H * s.nq;
     const dim3 grid((unsigned)((rows + kWarps - 1) / kWarps));
     if (dbg == 0) fwd_kernel<T, D, 0><<<grid, kWarps * 32, 0, st>>>(a, s);
     else if (dbg == 1) fwd_kernel<T, D, 1><<<grid, kWarps * 32, 0, st>>>(a, s);
@@ -379,7 +382,7 @@ static cudaError_t fwd_dispatch(const FwdArgs &a, const Shape &s, int dbg, cudaS
 
 template <typename T, int D>
 static cudaError_t bwd_run(const BwdArgs &a, const Shape &s, cudaStream_t st) {
-    const long long rows = (long long)s.B * s.H * s.N;
+    const long long rows = (long long)s.B * s.H * s.nq;
     const long long krows = (long long)s.B * s.Hkv * s.N;
     const dim3 g1((unsigned)((rows + kWarps - 1) / kWarps));
     const dim3 g2((unsigned)((krows + kWarps - 1) / kWarps));

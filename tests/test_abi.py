@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     for n in ("pi_attn_fwd", "pi_attn_fwd_f32", "pi_attn_bwd", "pi_attn_bwd_f32",
               "pi_attn_bwd_workspace_size", "pi_attn_status", "pi_attn_strerror",
               "pi_attn_debug_counts", "pi_attn_debug_probs", "pi_attn_debug_wait_timeout",
-              "pi_attn_decode", "pi_attn_bwd_noalloc", "pi_attn_debug_trace", "pi_attn_fwd_gated"):
+              "pi_attn_decode", "pi_attn_bwd_noalloc", "pi_attn_debug_trace", "pi_attn_fwd_gated",
+              "pi_attn_fwd_shard", "pi_attn_bwd_shard"):
         assert n in names
 
 
@@ -133,6 +134,36 @@ def test_bwd_validation(lib, fn):
     assert bwd_call(lib, mode=2, alpha=None, fn=fn) == PI_ERR_NULL   # bidirectional needs alpha
     assert bwd_call(lib, mode=2, ws=None, fn=fn) == PI_ERR_WORKSPACE  # validated like pi mode
     assert bwd_call(lib, mode=3, fn=fn) == PI_ERR_UNSUPPORTED
+
+
+def shard_fwd_call(lib, Nq=128, Nkv=384, off=256, mode=0, kl=8, S=1, q=A16, lse=A16):
+    return lib.pi_attn_fwd_shard(q, A16, A16, A16, 1, 2, 2, Nq, Nkv, off, 64, kl, 16, S, mode, A16, lse,
+                                 None)
+
+
+def shard_bwd_call(lib, Nq=128, Nkv=384, off=256, ws_bytes=1 << 20, dq=A16):
+    return lib.pi_attn_bwd_shard(A16, A16, A16, A16, A16, A16, A16, 1, 2, 2, Nq, Nkv, off, 64, 8, 16, 1, 0,
+                                 dq, A16, A16, A16, A16, ws_bytes, None)
+
+
+def test_shard_validation(lib):
+    """The query window [q_offset, q_offset + Nq) must lie inside the Nkv key rows and start on a
+    128-row boundary; the rest is validated as for the whole-sequence calls."""
+    assert shard_fwd_call(lib, off=-128) == PI_ERR_SHAPE
+    assert shard_fwd_call(lib, off=64) == PI_ERR_SHAPE
+    assert shard_fwd_call(lib, off=384) == PI_ERR_SHAPE          # window past the key rows
+    assert shard_fwd_call(lib, Nq=0) == PI_ERR_SHAPE
+    assert shard_fwd_call(lib, Nq=129) == PI_ERR_SHAPE           # 256 + 129 > 384
+    assert shard_fwd_call(lib, Nkv=0) == PI_ERR_SHAPE
+    assert shard_fwd_call(lib, q=None) == PI_ERR_NULL
+    assert shard_fwd_call(lib, lse=A16 + 2) == PI_ERR_ALIGN
+    assert shard_fwd_call(lib, mode=1, kl=16, S=1) == PI_ERR_SHAPE
+    assert shard_bwd_call(lib, off=64) == PI_ERR_SHAPE
+    assert shard_bwd_call(lib, dq=None) == PI_ERR_NULL
+    # the workspace holds one fp32 per query row of the shard (Nq), not per key row
+    need = lib.pi_attn_bwd_workspace_size(1, 2, 2, 128, 64)
+    assert need < lib.pi_attn_bwd_workspace_size(1, 2, 2, 384, 64)
+    assert shard_bwd_call(lib, ws_bytes=need - 1) == PI_ERR_WORKSPACE
 
 
 def dec_call(lib, q=A16, kc=A16, vc=A16, alpha=A16, B=1, H=4, Hkv=2, N=64, d=64, kl=8, per=16, S=1,
