@@ -16,8 +16,9 @@ Context Propagating Perceiver Architectures...", section 2, PAR block):
                                   skips i -/+ m*pi: the general form of the same page, 2.1-2.2)
   C7  bidirectional training bf16 B2 H16 Hkv16 N16384 d64  k256 pi512  S2, fwd+bwd (C5's
                                   shapes in the bidirectional form)
-  C8  gated long-context GQA     C4's layer with the fused gate: alpha = sigmoid(q . w_h + c_h)
-                                  computed in the forward launch (gate_weights(H, d, seed + 100))
+  C8  gated long-context GQA     C4's layer with the fused gate: alpha from the per-head MLP
+                                  sigmoid(w2_h . max(0, W1_h q + b1_h) + b2_h), computed in the
+                                  forward launch (gate_weights(H, d, seed + 100))
   D4  decode step, C4 layer       B64 H16 Hkv4 cache N16384 d128 k256 pi1024 S4: one new
                                   query per sequence (q [B,H,d], alpha [B,H]) against the cache
 

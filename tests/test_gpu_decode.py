@@ -126,3 +126,23 @@ def test_decode_alpha_edges():
     ro, rl = reference(q, k, v, a, kl, per, S, MODE_PI)
     close("out", out.float().cpu().numpy(), ro)
     close("lse", lse.cpu().numpy(), rl)
+
+
+def test_decode_at_the_d4_shape():
+    """The benchmarked decode step itself: D4's seeded inputs (64 sequences, 16 heads on 4 KV
+    heads, cache 16384, d 128, k 256, pi 1024, S 4) in the launch configuration the bench times.
+    Row N-1 attends only to the cache rows from N-1 - S*pi on, and the neighbour sets are the same
+    in any window that holds them, so the oracle runs on the last S*pi + 1 rows of the cache."""
+    from structured_sparse_long_gb300.synth import WORKLOADS, make_inputs
+    w = WORKLOADS["D4"]
+    inp = make_inputs(w, with_dout=False)
+    q, k, v, a = inp["q"], inp["k"], inp["v"], inp["alpha"]
+    assert tuple(k.shape) == (64, 4, 16384, 128) and tuple(q.shape) == (64, 16, 128)
+    out, lse = pa.decode(q.cuda(), k.cuda(), v.cuda(), a.cuda(), w.k_local, w.period, w.S, w.mode)
+    torch.cuda.synchronize()
+    assert pa.status() == 0
+    s0 = w.N - 1 - w.S * w.period
+    ro, rl = reference(q, k[:, :, s0:].contiguous(), v[:, :, s0:].contiguous(), a, w.k_local, w.period,
+                       w.S, w.mode)
+    close("out", out.float().cpu().numpy(), ro)
+    close("lse", lse.cpu().numpy(), rl)
