@@ -16,8 +16,9 @@
 //   * Warp w handles the query heads w, w+4, ... of the GQA group.  Lanes split d for the dot
 //     products (conflict-free 256-byte row reads), a butterfly reduce-scatter leaves lane t
 //     with the score of key t, and the warp keeps an online softmax state per head.
-//   * The P partial states (m, l, o) of a head are merged by CTA 0 of the cluster through
-//     distributed shared memory, which writes out (bf16) and lse.
+//   * The P partial states (m, l, o) of head hh are merged by CTA hh % P of the cluster through
+//     distributed shared memory (vector loads, all issued before use), which writes out (bf16)
+//     and lse.
 //   * Every mbarrier wait is bounded; a CTA that gives up still takes part in both cluster
 //     barriers, so its cluster never waits forever.
 #include <cuda.h>
@@ -57,7 +58,7 @@ struct Lay {
     static constexpr int ROW = D * 2;                       // bytes of one bf16 row
     static constexpr int STAGE = 2 * KEYS * ROW;            // K then V rows of one chunk
     static constexpr int PART_OFF = 2 * STAGE;              // partial states after the ring
-    static constexpr int PART = (D + 2) * 4;                // m, l, o[D] of one head (fp32)
+    static constexpr int PART = (D + 4) * 4;                // o[D], m, l of one head (fp32), 16-B rows
     static constexpr int BAR_OFF = PART_OFF + MAX_G * PART; // full[2], abort flag
     static constexpr int BYTES = BAR_OFF + 32;
 };
@@ -76,12 +77,23 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    return remote;
+}
+// Loads from another CTA's shared memory.  Volatile, so they stay after the cluster barrier and
+// in program order, but without a memory clobber, so a run of them is issued back to back.
+__device__ __forceinline__ void ld_dsmem2(uint32_t remote, float &x, float &y) {
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(x), "=f"(y) : "r"(remote));
+}
+template <int E>
+__device__ __forceinline__ void ld_dsmem_vec(uint32_t remote, float *f) {
+    if (E == 4)
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(remote));
+    else
+        ld_dsmem2(remote, f[0], f[1]);
 }
 
 // E consecutive bf16 of a shared-memory row (E = 2 or 4: one 4- or 8-byte load) as fp32.
@@ -258,36 +270,45 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     for (int j = 0; j < HPW; ++j) {
         const int hh = warp + WARPS * j;
         if (hh >= G) break;
-        float *ps = part + hh * (D + 2);
+        float *ps = part + hh * (D + 4);
         if (lane == 0) {
-            ps[0] = ok ? m[j] : -INFINITY;
-            ps[1] = ok ? l[j] : 0.f;
+            ps[D] = ok ? m[j] : -INFINITY;
+            ps[D + 1] = ok ? l[j] : 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < E; ++e) ps[2 + lane * E + e] = ok ? o[j][e] : 0.f;
+        for (int e = 0; e < E; ++e) ps[lane * E + e] = ok ? o[j][e] : 0.f;
     }
     cluster_sync();
-    if (r == 0) {
-        for (int hh = warp; hh < G; hh += WARPS) {
-            const uint32_t pa = sbase + L::PART_OFF + hh * (D + 2) * 4;
-            float mr[MAX_P];
-            float mt = -INFINITY;
-            for (int x = 0; x < P; ++x) {
-                mr[x] = ld_dsmem(pa, x);
-                mt = fmaxf(mt, mr[x]);
-            }
-            float lt = 0.f, ot[E];
+    // head hh is merged by CTA hh % P of the cluster, its warps taking those heads in turn; all
+    // P partial states of a head are loaded before any is used
+    for (int hh = r + P * warp; hh < G; hh += P * WARPS) {
+        const uint32_t pa = sbase + L::PART_OFF + hh * (D + 4) * 4;
+        float mr[MAX_P], lr[MAX_P], orr[MAX_P][E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) ot[e] = 0.f;
-            if (mt != -INFINITY) {
-                for (int x = 0; x < P; ++x) {
-                    if (mr[x] == -INFINITY) continue;
-                    const float f = exp2f(mr[x] - mt);
-                    lt += f * ld_dsmem(pa + 4, x);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) ot[e] += f * ld_dsmem(pa + (2 + lane * E + e) * 4, x);
-                }
+        for (int x = 0; x < MAX_P; ++x) {
+            if (x < P) {
+                ld_dsmem2(dsmem_addr(pa + D * 4, x), mr[x], lr[x]);
+                ld_dsmem_vec<E>(dsmem_addr(pa + lane * E * 4, x), orr[x]);
             }
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < MAX_P; ++x)
+            if (x < P) mt = fmaxf(mt, mr[x]);
+        float lt = 0.f, ot[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) ot[e] = 0.f;
+        if (mt != -INFINITY) {
+#pragma unroll
+            for (int x = 0; x < MAX_P; ++x) {
+                if (x >= P || mr[x] == -INFINITY) continue;
+                const float f = exp2f(mr[x] - mt);
+                lt = fmaf(f, lr[x], lt);
+#pragma unroll
+                for (int e = 0; e < E; ++e) ot[e] = fmaf(f, orr[x][e], ot[e]);
+            }
+        }
+        {
             const int h = g * G + hh;
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             __nv_bfloat16 *orow = a.out + ((size_t)b * s.H + h) * D + lane * E;
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
             if (lane == 0) a.lse[(size_t)b * s.H + h] = lt > 0.f ? (mt + log2f(lt)) * kLn2 : -INFINITY;
         }
     }
-    cluster_sync();  // the other CTAs' shared memory stays alive until CTA 0 has read it
+    cluster_sync();  // every CTA's shared memory stays alive until the others have read it
 }
 
 template <int D, int HPW>
