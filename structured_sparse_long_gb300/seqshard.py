@@ -10,7 +10,8 @@ sequence split into contiguous shards, one per rank, a shard's queries [t0, t1) 
     ECP    [(floor(t0 / c) - 1) * c, t1)                  (the previous half-segment)
 
 clipped to [0, N).  The rows of these sets that another rank owns are the shard's halo.  The
-forward receives them point to point (NCCL send/recv on GPUs; gloo in the tests), places them in
+forward receives them point to point (NCCL send/recv on GPUs; gloo, through host copies for device
+tensors, in the tests), places them in
 a local key/value window [w0, w1) (rows of the window that no query attends stay zero) and runs
 pi_attn_fwd_shard on it.  The backward runs pi_attn_bwd_shard, which gives the shard's part of
 the window rows' dk/dv, sends the halo rows' parts back to their owners and adds what it
@@ -156,6 +157,26 @@ def _run(ops):
             w.wait()
 
 
+def _staged(x: torch.Tensor, group) -> bool:
+    """Whether transfers of x go through host memory: gloo moves CPU tensors only."""
+    return x.is_cuda and dist.get_backend(group) == "gloo"
+
+
+def _exchange(sends, recvs, dtype, device, group, staged):
+    """Point-to-point transfers: sends = [(peer, tensor)], recvs = [(peer, shape)]; returns the
+    received tensors on `device`.  With staged, both sides of each transfer are host copies."""
+    ops, bufs = [], []
+    for peer, t in sends:
+        t = t.contiguous()
+        ops.append(dist.P2POp(dist.isend, t.cpu() if staged else t, _peer(group, peer), group))
+    for peer, shape in recvs:
+        buf = torch.empty(shape, dtype=dtype, device="cpu" if staged else device)
+        bufs.append(buf)
+        ops.append(dist.P2POp(dist.irecv, buf, _peer(group, peer), group))
+    _run(ops)
+    return [b.to(device) if staged else b for b in bufs]
+
+
 def gather_window(x_own: torch.Tensor, p: ShardPlan, group=None) -> torch.Tensor:
     """The window [w0, w1) of a [B, Hkv, rows, d] tensor from this rank's rows and the halo
     rows the peers send (rows of the window no query attends are zero)."""
@@ -164,16 +185,10 @@ def gather_window(x_own: torch.Tensor, p: ShardPlan, group=None) -> torch.Tensor
         raise ValueError(f"rank {p.rank} owns {p.n_rows} rows, got {n}")
     win = torch.zeros((B, Hkv, p.n_window, d), dtype=x_own.dtype, device=x_own.device)
     win[:, :, p.t0 - p.w0:p.t1 - p.w0] = x_own
-    ops, bufs = [], []
-    for pc in p.send:
-        ops.append(dist.P2POp(dist.isend, x_own[:, :, pc.a - p.t0:pc.b - p.t0].contiguous(),
-                              _peer(group, pc.peer), group))
-    for pc in p.recv:
-        buf = torch.empty((B, Hkv, pc.b - pc.a, d), dtype=x_own.dtype, device=x_own.device)
-        bufs.append((pc, buf))
-        ops.append(dist.P2POp(dist.irecv, buf, _peer(group, pc.peer), group))
-    _run(ops)
-    for pc, buf in bufs:
+    got = _exchange([(pc.peer, x_own[:, :, pc.a - p.t0:pc.b - p.t0]) for pc in p.send],
+                    [(pc.peer, (B, Hkv, pc.b - pc.a, d)) for pc in p.recv],
+                    x_own.dtype, x_own.device, group, _staged(x_own, group))
+    for pc, buf in zip(p.recv, got):
         win[:, :, pc.a - p.w0:pc.b - p.w0] = buf
     return win
 
@@ -186,16 +201,11 @@ def reduce_window_grad(g_win: torch.Tensor, p: ShardPlan, group=None) -> torch.T
         raise ValueError(f"rank {p.rank} has a {p.n_window}-row window, got {n}")
     acc = torch.float64 if g_win.dtype == torch.float64 else torch.float32
     own = g_win[:, :, p.t0 - p.w0:p.t1 - p.w0].to(acc)
-    ops, bufs = [], []
-    for pc in p.recv:  # rows received in the forward: their gradient parts go back
-        ops.append(dist.P2POp(dist.isend, g_win[:, :, pc.a - p.w0:pc.b - p.w0].contiguous(),
-                              _peer(group, pc.peer), group))
-    for pc in p.send:  # rows sent in the forward: the peers' parts come back
-        buf = torch.empty((B, Hkv, pc.b - pc.a, d), dtype=g_win.dtype, device=g_win.device)
-        bufs.append((pc, buf))
-        ops.append(dist.P2POp(dist.irecv, buf, _peer(group, pc.peer), group))
-    _run(ops)
-    for pc, buf in bufs:
+    # rows received in the forward send their gradient parts back; rows sent get the peers' parts
+    got = _exchange([(pc.peer, g_win[:, :, pc.a - p.w0:pc.b - p.w0]) for pc in p.recv],
+                    [(pc.peer, (B, Hkv, pc.b - pc.a, d)) for pc in p.send],
+                    g_win.dtype, g_win.device, group, _staged(g_win, group))
+    for pc, buf in zip(p.send, got):
         own[:, :, pc.a - p.t0:pc.b - p.t0] += buf.to(acc)
     return own.to(g_win.dtype)
 

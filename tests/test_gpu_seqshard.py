@@ -130,3 +130,79 @@ def test_shard_window_checks():
         with pytest.raises(pa.PiAttnError) as e:
             pa.fwd_shard(q, k, v, al, off, w.k_local, w.period, w.S, w.mode)
         assert e.value.code == -2  # PI_ERR_SHAPE
+
+
+# ---------------------------------------------------------------- two ranks through a process group
+
+def _rank(rank, world, port, case_idx, queue):
+    import os
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = CASES[case_idx][0]
+        inp = make_inputs(w, with_dout=True)
+        p = ss.plan(w.N, world, w.k_local, w.period, w.S, w.mode)[rank]
+        own = lambda t: None if t is None else t[:, :, p.t0:p.t1].contiguous().cuda()  # noqa: E731
+        out, lse, ctx = ss.forward(own(inp["q"]), own(inp["k"]), own(inp["v"]), own(inp["alpha"]), p,
+                                   w.k_local, w.period, w.S, w.mode)
+        grads = ss.backward(ctx, own(inp["dout"]))
+        torch.cuda.synchronize()
+        queue.put((rank, pa.status(), [t.cpu() for t in (out, lse) + tuple(grads)]))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case_idx", [0, 2])
+def test_two_ranks_exchange_halos_through_a_process_group(case_idx):
+    """Two ranks (gloo, both on this GPU; their kernels never wait on each other) each hold their
+    own rows, exchange halos with seqshard.forward/backward and run the shard kernels.  Their
+    results equal, bit for bit, the same plan carried out in one process: out, lse, dq and dalpha
+    the whole-sequence rows, dk and dv the owner's window part plus the parts returned to it, in
+    the plan's order, summed in fp32."""
+    import socket
+    import torch.multiprocessing as mp
+    w, _ = CASES[case_idx]
+    world = 2
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, case_idx, queue)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    res = {}
+    for _ in range(world):
+        r, st, ts = queue.get(timeout=600)
+        assert st == 0
+        res[r] = ts
+    for pr in procs:
+        pr.join(120)
+        assert pr.exitcode == 0
+
+    inp = make_inputs(w, with_dout=True)
+    d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    plans = ss.plan(w.N, world, w.k_local, w.period, w.S, w.mode)
+    parts = []
+    for p in plans:
+        rows = slice(p.t0, p.t1)
+        q = d["q"][:, :, rows].contiguous()
+        al = d["alpha"][:, :, rows].contiguous() if d["alpha"] is not None else None
+        kw, vw = ss.window_from_full(d["k"], p), ss.window_from_full(d["v"], p)
+        out, lse = pa.fwd_shard(q, kw, vw, al, p.q_offset, w.k_local, w.period, w.S, w.mode)
+        dq, dk, dv, dal = pa.bwd_shard(q, kw, vw, al, out, lse, d["dout"][:, :, rows].contiguous(),
+                                       p.q_offset, w.k_local, w.period, w.S, w.mode)
+        parts.append((out, lse, dq, dk, dv, dal))
+    torch.cuda.synchronize()
+    assert pa.status() == 0
+    for r, p in enumerate(plans):
+        got = res[r]
+        for j, name in ((0, "out"), (1, "lse"), (2, "dq"), (5, "dalpha")):
+            assert torch.equal(got[j], parts[r][j].cpu()), f"rank {r} {name}"
+        for j, name in ((3, "dk"), (4, "dv")):
+            own = parts[r][j][:, :, p.t0 - p.w0:p.t1 - p.w0].float()
+            for pc in p.send:  # the rows of this rank in the peer's window, back from the peer
+                q_plan = plans[pc.peer]
+                own[:, :, pc.a - p.t0:pc.b - p.t0] += parts[pc.peer][j][:, :, pc.a - q_plan.w0:pc.b - q_plan.w0].float()
+            assert torch.equal(got[j], own.to(torch.bfloat16).cpu()), f"rank {r} {name}"
