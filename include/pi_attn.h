@@ -121,9 +121,10 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
  * a logistic output:
  *     hid_f = max(0, sum_t gate_w1[h][f][t] q_{b,h,i,t} + gate_b1[h][f]),
  *     alpha_{b,h,i} = 1 / (1 + exp(-(sum_f gate_w2[h][f] hid_f + gate_b2[h]))),
- * computed in fp32 from the bf16 query row the kernel has already staged, then
- * used exactly as pi_attn_fwd uses its alpha input.
- *   gate_w1 [H, PI_ATTN_GATE_HIDDEN, d] fp32 (16-byte aligned), gate_b1 and gate_w2
+ * computed with the hidden pre-activations W1_h q on the tensor core (the block's query tile times the
+ * W1 rows of its heads, bf16 operands, fp32 accumulation; one extra key tile per block), the
+ * rest in fp32, then used exactly as pi_attn_fwd uses its alpha input.
+ *   gate_w1 [H, PI_ATTN_GATE_HIDDEN, d] bf16 (16-byte aligned), gate_b1 and gate_w2
  *   [H, PI_ATTN_GATE_HIDDEN] fp32, gate_b2 [H] fp32; alpha_out [B, H, N] fp32 (may be
  *   NULL; receives the gate's alpha, e.g. for pi_attn_bwd, whose dalpha is then the
  *   gradient with respect to these values; the gate's own weight gradients follow
@@ -132,7 +133,7 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
  *   arguments, layouts and errors as pi_attn_fwd.
  */
 #define PI_ATTN_GATE_HIDDEN 8
-int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w1,
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const void *gate_w1,
                       const float *gate_b1, const float *gate_w2, const float *gate_b2, int B,
                       int H, int Hkv, int N, int d, int k_local, int period, int S, int mode,
                       void *out, float *lse, float *alpha_out, void *stream);

@@ -161,13 +161,13 @@ def fwd_gated(q, k, v, gate, k_local: int, period: int, S: int, mode: int = MODE
               out=None, lse=None, alpha_out=None, stream=None):
     """pi_attn_fwd_gated (bf16, d 64 or 128): the forward with the gate computed in the same
     launch by the per-head MLP hid = max(0, W1_h q + b1_h), alpha = 1/(1 + exp(-(w2_h . hid + b2_h))).
-    gate = (W1 [H, 8, d], b1 [H, 8], w2 [H, 8], b2 [H]), fp32.  Returns (out, lse, alpha)."""
+    gate = (W1 [H, 8, d] bf16, b1 [H, 8], w2 [H, 8], b2 [H] fp32).  Returns (out, lse, alpha)."""
     B, H, Hkv, N, d = _sizes(q, k)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _expect(t, n, torch.bfloat16)
     _expect(v, "v", torch.bfloat16, k.shape)
     w1, b1, w2, b2 = gate
-    _expect(w1, "gate_w1", torch.float32, (H, GATE_HIDDEN, d))
+    _expect(w1, "gate_w1", torch.bfloat16, (H, GATE_HIDDEN, d))
     _expect(b1, "gate_b1", torch.float32, (H, GATE_HIDDEN))
     _expect(w2, "gate_w2", torch.float32, (H, GATE_HIDDEN))
     _expect(b2, "gate_b2", torch.float32, (H,))

@@ -187,7 +187,7 @@ int pi_attn_fwd_f32(const void *q, const void *k, const void *v, const float *al
                    0, nullptr, nullptr, nullptr, nullptr);
 }
 
-int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const float *gate_w1,
+int pi_attn_fwd_gated(const void *q, const void *k, const void *v, const void *gate_w1,
                       const float *gate_b1, const float *gate_w2, const float *gate_b2, int B, int H,
                       int Hkv, int N, int d, int k_local, int period, int S, int mode, void *out,
                       float *lse, float *alpha_out, void *stream) {

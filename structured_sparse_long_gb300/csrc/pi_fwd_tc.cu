@@ -233,8 +233,8 @@ struct TcArgs {
     float *P;
     long long *trace;  // DBG 3: clock64() stamps, kTraceSlots per traced CTA
     int n_trace;       // DBG 3: CTAs 0 .. n_trace-1 are traced
-    // fused gate (or null): hid = max(0, W1_h q_i + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h)))
-    const float *gate_w1;  // [H, kGateHidden, d]
+    // fused gate (GATE): hid = max(0, W1_h q_i + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h)));
+    // W1 [H * kGateHidden, d] bf16 reaches the kernel as a tensor map
     const float *gate_b1;  // [H, kGateHidden]
     const float *gate_w2;  // [H, kGateHidden]
     const float *gate_b2;  // [H]
@@ -329,19 +329,9 @@ __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc
 
 // This row of a Q tile (staged in shared memory, 128B-swizzled) into TMEM lane (the calling
 // thread's), columns Q_COL + w holding the bf16 pair (q[2w], q[2w+1]): the A operand layout
-// of the S products.  When w1 is not null it also evaluates the fused gate's network ("pi-
-// Attention" page, 2.3: a light MLP per token and per head) on the same words: the hidden
-// pre-activations W1_h q + b1_h, then the output logit w2_h . max(0, .) + b2_h, returned.  The
-// weights of a warp's rows are one head's, so their loads are warp-uniform.  One out-of-line
-// copy: it runs once per block.
-template <int D, bool GATE>
-static __device__ __noinline__ float copy_q_row(const uint8_t *qrow, int swz, uint32_t taddr, const float *w1,
-                                                const float *b1, const float *w2, float b2) {
-    float pre[kGateHidden];
-    if (GATE) {
-#pragma unroll
-        for (int f = 0; f < kGateHidden; ++f) pre[f] = b1[f];
-    }
+// of the S products.  One out-of-line copy: it runs once per block.
+template <int D>
+static __device__ __noinline__ void copy_q_row(const uint8_t *qrow, int swz, uint32_t taddr) {
 #pragma unroll 1
     for (int dc = 0; dc < D / 64; ++dc) {
         uint32_t wq[32];
@@ -352,43 +342,29 @@ static __device__ __noinline__ float copy_q_row(const uint8_t *qrow, int swz, ui
             wq[4 * ch + 1] = u4.y;
             wq[4 * ch + 2] = u4.z;
             wq[4 * ch + 3] = u4.w;
-            if (GATE) {
-                const float qv[8] = {__uint_as_float(u4.x << 16), __uint_as_float(u4.x & 0xffff0000u),
-                                     __uint_as_float(u4.y << 16), __uint_as_float(u4.y & 0xffff0000u),
-                                     __uint_as_float(u4.z << 16), __uint_as_float(u4.z & 0xffff0000u),
-                                     __uint_as_float(u4.w << 16), __uint_as_float(u4.w & 0xffff0000u)};
-#pragma unroll
-                for (int f = 0; f < kGateHidden; ++f) {
-                    const float *wr = w1 + f * D + dc * 64 + ch * 8;
-                    const float4 wa = *reinterpret_cast<const float4 *>(wr);
-                    const float4 wb = *reinterpret_cast<const float4 *>(wr + 4);
-                    pre[f] = fmaf(qv[0], wa.x, pre[f]);
-                    pre[f] = fmaf(qv[1], wa.y, pre[f]);
-                    pre[f] = fmaf(qv[2], wa.z, pre[f]);
-                    pre[f] = fmaf(qv[3], wa.w, pre[f]);
-                    pre[f] = fmaf(qv[4], wb.x, pre[f]);
-                    pre[f] = fmaf(qv[5], wb.y, pre[f]);
-                    pre[f] = fmaf(qv[6], wb.z, pre[f]);
-                    pre[f] = fmaf(qv[7], wb.w, pre[f]);
-                }
-            }
         }
         tmem_st16(taddr + dc * 32, wq);
         tmem_st16(taddr + dc * 32 + 16, wq + 16);
     }
+}
+
+// The fused gate's output for one row ("pi-Attention" page, 2.3: a light MLP per token and per
+// head): pre holds the row's hidden pre-activations W1_h q (the tensor core's product of the Q
+// tile with the W1 rows of the block's heads); returns alpha = 1 / (1 + exp(-z)) with
+// z = w2_h . max(0, pre + b1_h) + b2_h.  A warp's rows share one head, so the weight loads are
+// warp-uniform.
+__device__ __forceinline__ float gate_alpha(const uint32_t *pre, const float *b1, const float *w2, float b2) {
     float z = b2;
-    if (GATE) {
 #pragma unroll
-        for (int f = 0; f < kGateHidden; ++f) z = fmaf(w2[f], fmaxf(pre[f], 0.f), z);
-    }
-    return z;
+    for (int f = 0; f < kGateHidden; ++f) z = fmaf(w2[f], fmaxf(__uint_as_float(pre[f]) + b1[f], 0.f), z);
+    return 1.f / (1.f + __expf(-z));
 }
 
 template <int D, int DBG, bool GATE>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-              const TcArgs args) {
+              const __grid_constant__ CUtensorMap tmW, const TcArgs args) {
     using C = Cfg<D>;
     constexpr int KST = C::KSTAGES, VST = C::VSTAGES, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
@@ -470,12 +446,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tma_load_3d_hint(sbuf + st * C::KV_STAGE + dc * C::KV_DBLK, tm, dc * 64, key0, bd.b * s.Hkv + bd.g,
                              bar(full_bar + st), policy);
     };
+    // With the fused gate a block's first tile holds the W1 rows of its heads (32 rows of the
+    // [H * 8, d] bf16 matrix from row h0 * 8: its S product is the heads' hidden
+    // pre-activations); its key tiles follow, shifted by one.
+    constexpr int G0 = GATE ? 1 : 0;
+    auto issue_k = [&](const BlockDesc &bd, int t, int st, uint64_t policy) {
+        if (GATE && t == 0) {
+            mbar_expect_tx(bar(C::B_KF + st), C::KD * BOX_BYTES);
+            for (int dc = 0; dc < C::KD; ++dc)
+                tma_load_3d_hint(sK + st * C::KV_STAGE + dc * C::KV_DBLK, &tmW, dc * 64, bd.h0 * kGateHidden, 0,
+                                 bar(C::B_KF + st), policy);
+        } else {
+            issue_kv(&tmK, sK, C::B_KF, bd, t - G0, st, policy);
+        }
+    };
     // The first K tile, which the first S = Q K^T waits for, goes out before the CTA barrier, so
     // that its latency overlaps the TMEM allocation and the barrier itself.
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmK);
+        if (GATE) prefetch_tmap(&tmW);
         stamp_tile(8, 0);
-        issue_kv(&tmK, sK, C::B_KF, bd0, 0, 0, policy_evict_last());
+        issue_k(bd0, 0, 0, policy_evict_last());
     }
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
@@ -496,7 +487,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int L = L0; ok && L < args.n_blocks; L = next_block(L)) {
                 BlockDesc bd;
                 describe_block(L, args, bd);
-                for (int t = (L == L0) ? 1 : 0; t < bd.n_tiles; ++t, ++gk) {
+                for (int t = (L == L0) ? 1 : 0; t < bd.n_tiles + G0; ++t, ++gk) {
                     const int st = (int)(gk % KST);
                     const uint32_t round = gk / KST;
                     if (round > 0 && !wait_bar(bar(C::B_KE + st), (round - 1) & 1, wc)) {
@@ -504,7 +495,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         break;
                     }
                     if (L == L0) stamp_tile(8, t);
-                    issue_kv(&tmK, sK, C::B_KF, bd, t, st, reused);
+                    issue_k(bd, t, st, reused);
                 }
             }
             if (*abort_flag) {  // let loads in flight land before the CTA leaves
@@ -599,7 +590,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_QT), (uint32_t)(k & 1), wc));
             if (!ok) break;
             if (k == 0 && lane == 0) stamp(3);
-            for (int t = 0; t < bd.n_tiles; ++t, ++gs) {
+            for (int t = 0; t < bd.n_tiles + G0; ++t, ++gs) {
                 const int st = (int)(gs % KST), buf = (int)(gs % NB);
                 bool w = timed_wait(bar(C::B_KF + st), (gs / KST) & 1, 104, t);
                 // buffer buf last held P of tile gs - NB: its PV must be done
@@ -639,20 +630,35 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ================= PV issuer: O += P V with P read from TMEM (whole warp, one elected
         // lane issuing, as for the S issuer)
         const uint32_t idesc = idesc_bf16(BM, D, 0, 1);
-        uint32_t gp = 0;
+        uint32_t gp = 0, gv = 0;  // tiles (S buffers) and V tiles, counted across blocks
         int k = 0;
         bool ok = true;
         for (int L = L0; ok && L < args.n_blocks; L = next_block(L), ++k) {
             BlockDesc bd;
             describe_block(L, args, bd);
-            for (int u = 0; u < bd.n_tiles; ++u, ++gp) {
-                const int st = (int)(gp % VST), buf = (int)(gp % NB);
+            for (int u = 0; u < bd.n_tiles + G0; ++u, ++gp) {
+                const int buf = (int)(gp % NB);
+                if (GATE && u == 0) {
+                    // the gate tile has no PV product: its buffer is free once the row threads
+                    // have read it (a commit with nothing new behind it)
+                    const bool w = wait_bar(bar(C::B_PR + buf), (gp / NB) & 1, wc);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (elect_one()) tc_commit(bar(C::B_PV + buf));
+                    __syncwarp();
+                    continue;
+                }
+                const int st = (int)(gv % VST);
                 bool w = timed_wait(bar(C::B_PR + buf), (gp / NB) & 1, 136, u);
-                if (w) w = timed_wait(bar(C::B_VF + st), (gp / VST) & 1, 152, u);
+                if (w) w = timed_wait(bar(C::B_VF + st), (gv / VST) & 1, 152, u);
                 if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
                     break;
                 }
+                ++gv;
                 tc_fence_after();
                 const uint32_t aP = tbase + buf * CHUNK;
                 const uint64_t b0 = sdesc(sV + st * C::KV_STAGE, C::KV_DBLK, 1024);
@@ -662,10 +668,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
                         mma_ts(tbase + C::O_COL, aP + kk * 8, b0 + (uint64_t)((kk * 16 * ROW_BYTES) >> 4), idesc,
-                               (u > 0 || kk > 0) ? 1u : 0u);
+                               (u > G0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(C::B_PV + buf));
                     tc_commit(bar(C::B_VE + st));
-                    if (u == bd.n_tiles - 1) tc_commit(bar(C::B_OF));
+                    if (u == bd.n_tiles + G0 - 1) tc_commit(bar(C::B_OF));
                 }
                 __syncwarp();
                 if (k == 0 && lane == 0) stamp_tile(56, u);
@@ -686,29 +692,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const float sc = s.scale_log2;
 
         // This row of block bd's Q tile into TMEM (rows past N hold the TMA's zero fill).
-        // Returns the row's alpha: the input's, or the fused gate's 1 / (1 + exp(-logit)).  The
-        // input's is loaded after the out-of-line copy (a load in flight across a call would
-        // be waited for there); it was prefetched into L2 a block ahead.
+        // Returns the row's input alpha (the fused gate's comes from the block's gate tile),
+        // loaded after the out-of-line copy (a load in flight across a call would be waited for
+        // there); it was prefetched into L2 a block ahead.
         auto copy_q = [&](const BlockDesc &bd, int kb, float &al_out) -> bool {
             const int iq = bd.p0 - s.qoff + trow, h = bd.h0 + hh;
             const bool row_ok = iq < s.nq;
             const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), (uint32_t)(kb & 1), wc))) return false;
-            constexpr bool gated = GATE;
-            const float z = copy_q_row<D, GATE>(
-                smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL,
-                gated ? args.gate_w1 + (size_t)h * kGateHidden * D : nullptr,
-                gated ? args.gate_b1 + h * kGateHidden : nullptr, gated ? args.gate_w2 + h * kGateHidden : nullptr,
-                gated ? args.gate_b2[h] : 0.f);
+            copy_q_row<D>(smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_QT));
-            if (gated) {
-                al_out = 1.f / (1.f + __expf(-z));
-                if (args.alpha_out && row_ok) args.alpha_out[row_g] = al_out;
-            } else {
-                al_out = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
-            }
+            if (!GATE) al_out = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
             return true;
         };
 
@@ -723,9 +719,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int i = bd.p0 + trow, h = bd.h0 + hh, iq = i - s.qoff;
             const bool row_ok = iq < s.nq;
             const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
-            const float al = al_next;
-            const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
-            const float off_skip = log2f(1.f - al);
+            float al = al_next;  // the fused gate sets it at the block's first tile
+            float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
+            float off_skip = log2f(1.f - al);
             const int lo_i = band_lo(i, s.mode, s.k_local);
             const int hi_i = band_hi(i, s.N, s.mode, s.k_local);
             float lse2_in = 0.f;
@@ -742,7 +738,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     prefetch_l2(args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.nq + in);
             }
 
-            for (int t = 0; t < bd.n_tiles; ++t, ++gsm) {
+            for (int t = 0; t < bd.n_tiles + G0; ++t, ++gsm) {
                 const int buf = (int)(gsm % NB);
                 if (DBG == 3 && warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (gsm / NB) & 1, 168, t);
                 else ok = wait_bar(bar(C::B_SF + buf), (gsm / NB) & 1, wc);
@@ -751,6 +747,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (k == 0 && warp == 4 && lane == 0) stamp_tile(72, t);
                 tc_fence_after();
                 __syncwarp();
+                if (GATE && t == 0) {
+                    // the gate tile: this row's head's 8 hidden pre-activations, then alpha
+                    uint32_t pre[kGateHidden];
+                    tmem_ld8(tbase + lane_base + buf * CHUNK + hh * kGateHidden, pre);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_PR + buf));  // the buffer is free for the next S
+                    al = gate_alpha(pre, args.gate_b1 + h * kGateHidden, args.gate_w2 + h * kGateHidden,
+                                    args.gate_b2[h]);
+                    if (args.alpha_out && row_ok) args.alpha_out[row_g] = al;
+                    off_band = log2f(al);
+                    off_skip = log2f(1.f - al);
+                    continue;
+                }
+                const int tk = t - G0;  // key tile of the block
                 const uint32_t tS = tbase + lane_base + buf * CHUNK;
                 uint32_t ra[CHUNK];
                 tmem_ld32(tS, ra);
@@ -761,7 +772,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // the maximum is only needed when some P exceeds 2^8 (the lazy-rescale bound),
                 // which a sum above 2^8 is the first sign of.  Rows with no reference yet take the
                 // general path, as do the debug modes that record per-row ranges.
-                const bool fast = (DBG == 0 || DBG == 3) && t >= bd.full_lo && t <= bd.full_hi &&
+                const bool fast = (DBG == 0 || DBG == 3) && tk >= bd.full_lo && tk <= bd.full_hi &&
                                   __all_sync(0xffffffffu, m_ref != -INFINITY);
                 float corr = 1.f, lsum, bo;
                 bool need_o = false, diag = false;
@@ -772,7 +783,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 } else {
                     int back, chi;
                     bool sk;
-                    const int key0 = bd.cw.key0(t, back, sk);
+                    const int key0 = bd.cw.key0(tk, back, sk);
                     float off;
                     if (!sk) {
                         clo = max(lo_i - key0, 0);
@@ -790,7 +801,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (mt > m_ref + kRescaleThreshold) {
                         if (m_ref != -INFINITY) {
                             corr = fast_exp2(m_ref - mt);
-                            need_o = (t > 0);
+                            need_o = (tk > 0);
                         }
                         m_ref = mt;
                     }
@@ -951,7 +962,8 @@ __global__ void wait_timeout_probe_kernel(int *status, uint64_t timeout_ns) {
 
 template <int D, int DBG, bool GATE = false>
 static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          const CUtensorMap &mo, const TcArgs &a, unsigned grid, cudaStream_t st) {
+                          const CUtensorMap &mo, const CUtensorMap &mw, const TcArgs &a, unsigned grid,
+                          cudaStream_t st) {
     constexpr int smem = Cfg<D>::SMEM_BYTES;
     static PerDeviceOnce configured;
     int dev = 0;
@@ -962,7 +974,7 @@ static cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CU
         if (e != cudaSuccess) return e;
         configured.mark(dev);
     }
-    fwd_tc_kernel<D, DBG, GATE><<<grid, NUM_THREADS, smem, st>>>(mq, mk, mv, mo, a);
+    fwd_tc_kernel<D, DBG, GATE><<<grid, NUM_THREADS, smem, st>>>(mq, mk, mv, mo, mw, a);
     return cudaGetLastError();
 }
 
@@ -1002,7 +1014,7 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     const int cpb_log2 = (R == 128) ? 2 : (R == 64) ? 1 : 0;
     TcArgs a{L.alpha, L.lse, s, GP, m_first, nqb, ngrp, R, cpb_log2, make_fastdiv(nqb), make_fastdiv(ngrp),
              make_fastdiv(G), make_fastdiv(s.S > 0 && s.period > 0 ? s.period : 1), n_blocks, L.status,
-             L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P, L.trace, L.n_trace, L.gate_w1, L.gate_b1, L.gate_w2,
+             L.timeout_ns, L.cnt, L.isum, L.lse_in, L.P, L.trace, L.n_trace, L.gate_b1, L.gate_w2,
              L.gate_b2, L.alpha_out};
     // The forward runs persistent, two CTAs per SM; the debug modes take one CTA per block.
     unsigned grid = (unsigned)n_blocks;
@@ -1012,21 +1024,23 @@ cudaError_t launch_fwd_tc(const LaunchFwd &L, cudaStream_t st) {
     }
     if (L.gate_w1) {  // the fused gate: the forward only
         if (L.dbg != 0) return cudaErrorInvalidValue;
-        if (s.d == 64) return launch<64, 0, true>(mq, mk, mv, mo, a, grid, st);
-        if (s.d == 128) return launch<128, 0, true>(mq, mk, mv, mo, a, grid, st);
+        CUtensorMap mw;  // W1 as [1][H * kGateHidden][d]: a block's heads are 32 (or fewer) rows
+        if (!make_map(&mw, L.gate_w1, s.d, s.H * kGateHidden, 1, CHUNK, 1)) return cudaErrorNotSupported;
+        if (s.d == 64) return launch<64, 0, true>(mq, mk, mv, mo, mw, a, grid, st);
+        if (s.d == 128) return launch<128, 0, true>(mq, mk, mv, mo, mw, a, grid, st);
         return cudaErrorInvalidValue;
     }
     if (s.d == 64) {
-        if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, a, grid, st);
-        if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, a, grid, st);
-        if (L.dbg == 3) return launch<64, 3>(mq, mk, mv, mo, a, grid, st);
-        return launch<64, 2>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 0) return launch<64, 0>(mq, mk, mv, mo, mk, a, grid, st);
+        if (L.dbg == 1) return launch<64, 1>(mq, mk, mv, mo, mk, a, grid, st);
+        if (L.dbg == 3) return launch<64, 3>(mq, mk, mv, mo, mk, a, grid, st);
+        return launch<64, 2>(mq, mk, mv, mo, mk, a, grid, st);
     }
     if (s.d == 128) {
-        if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, a, grid, st);
-        if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, a, grid, st);
-        if (L.dbg == 3) return launch<128, 3>(mq, mk, mv, mo, a, grid, st);
-        return launch<128, 2>(mq, mk, mv, mo, a, grid, st);
+        if (L.dbg == 0) return launch<128, 0>(mq, mk, mv, mo, mk, a, grid, st);
+        if (L.dbg == 1) return launch<128, 1>(mq, mk, mv, mo, mk, a, grid, st);
+        if (L.dbg == 3) return launch<128, 3>(mq, mk, mv, mo, mk, a, grid, st);
+        return launch<128, 2>(mq, mk, mv, mo, mk, a, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -42,7 +42,7 @@ struct LaunchFwd {
     // fused gate (tensor-core path): alpha from the per-head MLP of one hidden layer,
     // hid = max(0, W1_h q_i + b1_h), alpha = 1 / (1 + exp(-(w2_h . hid + b2_h))), computed in
     // the kernel instead of read from alpha; alpha_out (may be null) receives it
-    const float *gate_w1 = nullptr;  // [H, kGateHidden, d]
+    const void *gate_w1 = nullptr;   // [H, kGateHidden, d] bf16
     const float *gate_b1 = nullptr;  // [H, kGateHidden]
     const float *gate_w2 = nullptr;  // [H, kGateHidden]
     const float *gate_b2 = nullptr;  // [H]

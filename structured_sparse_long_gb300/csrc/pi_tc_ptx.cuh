@@ -196,6 +196,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
         : PI_R8(0), PI_R8(8), PI_R8(16), PI_R8(24)
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : PI_R8(0)
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "

@@ -166,12 +166,13 @@ GATE_HIDDEN = 8  # hidden units per head of the fused gate
 
 
 def gate_weights(H: int, d: int, seed: int):
-    """Synthetic weights of the fused gate's per-head MLP, fp32: W1 [H, 8, d] ~ N(0, 1/d) and
-    b1 [H, 8] ~ N(0, 1/4), so that for unit-variance queries the hidden pre-activations have
-    about unit spread; w2 [H, 8] ~ N(0, 2/8) and b2 [H] ~ N(0, 1), so that the output logit
-    spreads over about one unit and alpha covers (0, 1) without saturating."""
+    """Synthetic weights of the fused gate's per-head MLP: W1 [H, 8, d] ~ N(0, 1/d) drawn in fp32
+    and cast to bf16 (the tensor-core operand) and b1 [H, 8] ~ N(0, 1/4), so that for
+    unit-variance queries the hidden pre-activations have about unit spread; w2 [H, 8] ~ N(0, 2/8)
+    and b2 [H] ~ N(0, 1), fp32, so that the output logit spreads over about one unit and alpha
+    covers (0, 1) without saturating."""
     gen = torch.Generator().manual_seed(seed)
-    w1 = torch.randn(H, GATE_HIDDEN, d, generator=gen, dtype=torch.float32) / math.sqrt(d)
+    w1 = (torch.randn(H, GATE_HIDDEN, d, generator=gen, dtype=torch.float32) / math.sqrt(d)).to(torch.bfloat16)
     b1 = 0.5 * torch.randn(H, GATE_HIDDEN, generator=gen, dtype=torch.float32)
     w2 = torch.randn(H, GATE_HIDDEN, generator=gen, dtype=torch.float32) * math.sqrt(2.0 / GATE_HIDDEN)
     b2 = torch.randn(H, generator=gen, dtype=torch.float32)
