@@ -31,6 +31,9 @@
 //     adds the prior, keeps the running max m and sum l (rescaling O in TMEM only
 //     when the max grows by more than 2^8), writes P as bf16 over its S, and at
 //     the end of the block normalises O and stages it in shared memory.
+//   * The fused gate (GATE) puts one more tile in front of a block's key tiles: the
+//     W1 rows of the block's heads, so that its S product is the heads' hidden
+//     pre-activations; the row threads finish the MLP and take its alpha.
 //   * Every wait is bounded; a wait that runs out sets the device status word and
 //     the CTA unwinds without hanging.
 //   * The kernel's speed is bound by latency and by instruction fetch, so the
