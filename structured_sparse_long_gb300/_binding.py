@@ -3,7 +3,8 @@
 Every function here takes torch CUDA tensors, checks that their dtype, layout
 and device match what the C ABI expects, and passes raw device pointers, sizes
 and the current CUDA stream to the entry point of the same name in
-include/pi_attn.h.  All computation runs in the library's CUDA kernels; there
+include/pi_attn.h.  Calls only enqueue work; with check=True a compute call also
+synchronises its stream and raises if a device-side bounded wait gave up.  All computation runs in the library's CUDA kernels; there
 is no fallback: if the library is not built or cannot be loaded, every call
 raises.
 """
@@ -87,9 +88,15 @@ def strerror(code: int) -> str:
     return load().pi_attn_strerror(int(code)).decode()
 
 
-def _check(fn: str, code: int):
+def _check(fn: str, code: int, stream=None, check: bool = False):
+    """Raise on a launch error; with check, also synchronise the stream and raise if a device-side
+    bounded wait gave up (the status word, read and cleared by pi_attn_status)."""
     if code != PI_OK:
         raise PiAttnError(fn, code, strerror(code))
+    if check:
+        st = status(stream)
+        if st != PI_OK:
+            raise PiAttnError(fn, st, strerror(st))
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -129,7 +136,7 @@ def _sizes(q, k):
 
 
 def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
-        out=None, lse=None, stream=None):
+        out=None, lse=None, stream=None, check=False):
     """pi_attn_fwd (bf16) / pi_attn_fwd_f32 (fp32), chosen by q.dtype. Returns (out, lse)."""
     B, H, Hkv, N, d = _sizes(q, k)
     dt = q.dtype
@@ -150,7 +157,7 @@ def fwd(q, k, v, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
         raise ValueError(f"unsupported dtype {dt}")
     rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, N, d, k_local, period, S, mode,
             _ptr(out), _ptr(lse), _stream(stream))
-    _check(fn.__name__, rc)
+    _check(fn.__name__, rc, stream, check)
     return out, lse
 
 
@@ -158,7 +165,7 @@ GATE_HIDDEN = 8  # PI_ATTN_GATE_HIDDEN in include/pi_attn.h
 
 
 def fwd_gated(q, k, v, gate, k_local: int, period: int, S: int, mode: int = MODE_PI,
-              out=None, lse=None, alpha_out=None, stream=None):
+              out=None, lse=None, alpha_out=None, stream=None, check=False):
     """pi_attn_fwd_gated (bf16, d 64 or 128): the forward with the gate computed in the same
     launch by the per-head MLP hid = max(0, W1_h q + b1_h), alpha = 1/(1 + exp(-(w2_h . hid + b2_h))).
     gate = (W1 [H, 8, d] bf16, b1 [H, 8], w2 [H, 8], b2 [H] fp32).  Returns (out, lse, alpha)."""
@@ -184,12 +191,12 @@ def fwd_gated(q, k, v, gate, k_local: int, period: int, S: int, mode: int = MODE
     rc = lib.pi_attn_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), B, H, Hkv,
                                N, d, k_local, period, S, mode, _ptr(out), _ptr(lse), _ptr(alpha_out),
                                _stream(stream))
-    _check("pi_attn_fwd_gated", rc)
+    _check("pi_attn_fwd_gated", rc, stream, check)
     return out, lse, alpha_out
 
 
 def decode(q, k_cache, v_cache, alpha, k_local: int, period: int, S: int, mode: int = MODE_PI,
-           out=None, lse=None, stream=None):
+           out=None, lse=None, stream=None, check=False):
     """pi_attn_decode: q [B,H,d] bf16 against the cache k_cache/v_cache [B,Hkv,N,d] bf16
     (row N-1 of the forward). Returns (out [B,H,d], lse [B,H])."""
     if q.dim() != 3 or k_cache.dim() != 4:
@@ -209,7 +216,7 @@ def decode(q, k_cache, v_cache, alpha, k_local: int, period: int, S: int, mode: 
     _expect(lse, "lse", torch.float32, (B, H))
     rc = load().pi_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(alpha), B, H, Hkv, N, d,
                                k_local, period, S, mode, _ptr(out), _ptr(lse), _stream(stream))
-    _check("pi_attn_decode", rc)
+    _check("pi_attn_decode", rc, stream, check)
     return out, lse
 
 
@@ -233,7 +240,7 @@ def _grad_buffers(q, k, v, dq, dk, dv, dalpha):
 
 
 def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode: int = MODE_PI,
-        dq=None, dk=None, dv=None, dalpha=None, workspace=None, stream=None):
+        dq=None, dk=None, dv=None, dalpha=None, workspace=None, stream=None, check=False):
     """pi_attn_bwd (bf16) / pi_attn_bwd_f32, chosen by q.dtype. Returns (dq, dk, dv, dalpha)."""
     B, H, Hkv, N, d = _sizes(q, k)
     dt = q.dtype
@@ -258,12 +265,12 @@ def bwd(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int, mode:
     rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse), _ptr(dout),
             B, H, Hkv, N, d, k_local, period, S, mode, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(fn.__name__, rc)
+    _check(fn.__name__, rc, stream, check)
     return dq, dk, dv, dalpha
 
 
 def bwd_noalloc(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: int,
-                mode: int = MODE_PI, dq=None, dk=None, dv=None, dalpha=None, stream=None):
+                mode: int = MODE_PI, dq=None, dk=None, dv=None, dalpha=None, stream=None, check=False):
     """pi_attn_bwd_noalloc (bf16): the backward with the library's fixed device scratch
     instead of a caller workspace.  Returns (dq, dk, dv, dalpha)."""
     B, H, Hkv, N, d = _sizes(q, k)
@@ -278,7 +285,7 @@ def bwd_noalloc(q, k, v, alpha, out, lse, dout, k_local: int, period: int, S: in
     rc = load().pi_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(out), _ptr(lse),
                                     _ptr(dout), B, H, Hkv, N, d, k_local, period, S, mode,
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _stream(stream))
-    _check("pi_attn_bwd_noalloc", rc)
+    _check("pi_attn_bwd_noalloc", rc, stream, check)
     return dq, dk, dv, dalpha
 
 
@@ -290,7 +297,7 @@ def _shard_sizes(q, k):
 
 
 def fwd_shard(q, k, v, alpha, q_offset: int, k_local: int, period: int, S: int, mode: int = MODE_PI,
-              out=None, lse=None, stream=None):
+              out=None, lse=None, stream=None, check=False):
     """pi_attn_fwd_shard (bf16): the queries q [B,H,Nq,d] of a sequence shard, the first at key
     row q_offset of the local key/value window k, v [B,Hkv,Nkv,d].  Returns (out, lse)."""
     B, H, Hkv, Nq, Nkv, d = _shard_sizes(q, k)
@@ -308,13 +315,13 @@ def fwd_shard(q, k, v, alpha, q_offset: int, k_local: int, period: int, S: int, 
     rc = load().pi_attn_fwd_shard(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, Hkv, Nq, Nkv,
                                   int(q_offset), d, k_local, period, S, mode, _ptr(out), _ptr(lse),
                                   _stream(stream))
-    _check("pi_attn_fwd_shard", rc)
+    _check("pi_attn_fwd_shard", rc, stream, check)
     return out, lse
 
 
 def bwd_shard(q, k, v, alpha, out, lse, dout, q_offset: int, k_local: int, period: int, S: int,
               mode: int = MODE_PI, dq=None, dk=None, dv=None, dalpha=None, workspace=None,
-              stream=None):
+              stream=None, check=False):
     """pi_attn_bwd_shard (bf16).  Returns (dq, dk, dv, dalpha): dq and dalpha of the shard's
     queries, dk and dv [B,Hkv,Nkv,d] the shard's part of the window rows' gradients."""
     B, H, Hkv, Nq, Nkv, d = _shard_sizes(q, k)
@@ -336,7 +343,7 @@ def bwd_shard(q, k, v, alpha, out, lse, dout, q_offset: int, k_local: int, perio
                                   _ptr(dout), B, H, Hkv, Nq, Nkv, int(q_offset), d, k_local, period,
                                   S, mode, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
                                   _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("pi_attn_bwd_shard", rc)
+    _check("pi_attn_bwd_shard", rc, stream, check)
     return dq, dk, dv, dalpha
 
 

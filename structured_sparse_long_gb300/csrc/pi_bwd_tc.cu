@@ -834,15 +834,15 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             if (!key_ok) { clo = QC; chi = -1; }
             const float *xb = xvec + st * 2 * QC;
 #pragma unroll
-            for (int q = 0; q < QC / 16; ++q) {
-                uint32_t sr[16], dr[16];
-                tmem_ld16(bcol + C::ST_COL + q * 16, sr);
-                tmem_ld16(bcol + C::DPT_COL + q * 16, dr);
+            for (int q = 0; q < QC / 32; ++q) {  // 32 columns of S^T and dP^T per TMEM round trip
+                uint32_t sr[32], dr[32];
+                tmem_ld32(bcol + C::ST_COL + q * 32, sr);
+                tmem_ld32(bcol + C::DPT_COL + q * 32, dr);
                 tmem_wait_ld();
-                uint32_t pp[8], pz[8];
+                uint32_t pp[16], pz[16];
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    const int c0 = q * 16 + c;
+                for (int c = 0; c < 32; c += 2) {
+                    const int c0 = q * 32 + c;
                     const float2 bias = *reinterpret_cast<const float2 *>(xb + c0);
                     const float2 dd = *reinterpret_cast<const float2 *>(xb + QC + c0);
                     const bool v0 = c0 >= clo && c0 <= chi, v1 = c0 + 1 >= clo && c0 + 1 <= chi;
@@ -853,8 +853,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     pp[c / 2] = pack_bf16(p0, p1);
                     pz[c / 2] = pack_bf16(z0, z1);
                 }
-                tmem_st8(bcol + C::ST_COL + q * 8, pp);
-                tmem_st8(bcol + C::DPT_COL + q * 8, pz);
+                tmem_st16(bcol + C::ST_COL + q * 16, pp);
+                tmem_st16(bcol + C::DPT_COL + q * 16, pz);
             }
             tmem_wait_st();
             tc_fence_before();

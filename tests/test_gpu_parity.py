@@ -340,6 +340,22 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     check_forward(WORKLOADS["C1"])  # the context is still usable
 
 
+def test_checked_call_raises_on_a_device_timeout():
+    """check=True: the call synchronises and raises PI_ERR_DEVICE_TIMEOUT when the status word
+    holds a bounded wait that gave up (here the probe's); the next checked call is clean."""
+    w = small_case("chk", 1, 2, 2, 200, 64, 16, 32, 2, MODE_PI, "bf16", seed=5)
+    inp = make_inputs(w, with_dout=False)
+    d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    pa.debug_wait_timeout(2000)
+    with pytest.raises(pa.PiAttnError) as e:
+        pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, check=True)
+    assert e.value.code == -7
+    out, lse = pa.fwd(d["q"], d["k"], d["v"], d["alpha"], w.k_local, w.period, w.S, w.mode, check=True)
+    ref_out, ref_lse = oracle.fwd(inp["q"], inp["k"], inp["v"], inp["alpha"], w.k_local, w.period, w.S,
+                                  w.mode)
+    assert_close("out", out.float().cpu().numpy(), ref_out, "bf16")
+
+
 def test_trace_mode_matches_forward_and_stamps_are_ordered():
     """pi_attn_debug_trace runs the same forward: identical out/lse, and per-tile stamps of
     the softmax warp (one clock) are in order."""
