@@ -280,16 +280,25 @@ BWD_CASES = [
     ("bwd-bi-long-d128", 1, 4, 1, 1500, 128, 100, 256, 3, MODE_PI_BIDIR, "bf16"),
     ("bwd-bi-f32", 1, 2, 1, 120, 64, 16, 24, 3, MODE_PI_BIDIR, "f32"),
     ("bwd-bi-d32", 1, 2, 2, 100, 32, 10, 15, 2, MODE_PI_BIDIR, "bf16"),
+    # blocks whose number of skip multiples grows along the sequence (1 to 6; bidirectional:
+    # backward and forward multiples), in one launch
+    ("bwd-mixed-skip", 1, 2, 2, 700, 64, 20, 64, 6, MODE_PI, "bf16"),
+    ("bwd-bi-mixed-d128", 1, 4, 4, 600, 128, 30, 100, 3, MODE_PI_BIDIR, "bf16"),
+    # four query heads per KV head with one skip multiple; 1/sqrt(d) inputs keep dv (a sum over
+    # 4 heads) below 8, where bf16 storage alone stays inside the max-abs bound
+    ("bwd-gqa4-S1", 1, 8, 2, 300, 128, 40, 64, 1, MODE_PI, "bf16", "inv_sqrt_d"),
 ]
 
 
 @pytest.mark.parametrize("spec", BWD_CASES, ids=[s[0] for s in BWD_CASES])
 def test_small_backward(spec):
-    name, B, H, Hkv, N, d, k, per, S, mode, dt = spec
+    name, B, H, Hkv, N, d, k, per, S, mode, dt = spec[:11]
+    scale = spec[11] if len(spec) > 11 else "unit"
     # fp32 cases draw alpha as the fp32 workload C1 does, U(0.2, 0.8): dalpha carries the factor
     # 1/(alpha (1 - alpha)), and the fp32 bound is absolute
     a_spec = "none" if mode == MODE_ECP else ("uniform(0.2,0.8)" if dt == "f32" else "sigmoid(1.0)")
-    w = small_case(name, B, H, Hkv, N, d, k, per, S, mode, dt, seed=9, alpha=a_spec, backward=True)
+    w = small_case(name, B, H, Hkv, N, d, k, per, S, mode, dt, seed=9, qkv_scale=scale, alpha=a_spec,
+                   backward=True)
     inp = make_inputs(w, with_dout=True)
     dev = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
     out, lse = pa.fwd(dev["q"], dev["k"], dev["v"], dev["alpha"], k, per, S, mode)
