@@ -18,15 +18,16 @@
 //     "diagonal").
 //   * The kernel is persistent: each CTA (two per SM) processes blocks c,
 //     c + gridDim.x, ... in turn.  The next block's Q tile is loaded during the
-//     current block and copied into TMEM as soon as the current block's last S
-//     product is done, so the next block's first S products overlap this block's
-//     epilogue; a producer warp TMA-stores each block's staged output.
+//     current block and copied into TMEM (tcgen05.cp, by the S issuer) as soon as
+//     the current block's last S product is done, so the next block's first S
+//     products overlap this block's epilogue; a producer warp TMA-stores each
+//     block's staged output.
 //   * Warp 0 (lane 0) streams the K tiles; warp 2 (lane 0) streams the V tiles,
-//     stores the staged outputs and loads the next Q tiles.  The row threads copy
-//     each Q tile from shared memory into TMEM, so that both MMAs take their A
-//     operand from TMEM: warp 1 issues S = Q K^T into one of NB TMEM S buffers and
-//     warp 3 issues O += P V with P read from TMEM (each whole warp runs its loop,
-//     one elected lane issues the MMAs and commits).
+//     stores the staged outputs and loads the next Q tiles.  Both MMAs take their
+//     A operand from TMEM: warp 1 copies each Q tile there and issues S = Q K^T
+//     into one of NB TMEM S buffers, and warp 3 issues O += P V with P read from
+//     TMEM (each whole warp runs its loop, one elected lane issues the copies, the
+//     MMAs and the commits).
 //   * Warps 4-7 run the softmax, one thread per row (TMEM lane = row): masks,
 //     adds the prior, keeps the running max m and sum l (rescaling O in TMEM only
 //     when the max grows by more than 2^8), writes P as bf16 over its S, and at
@@ -84,9 +85,8 @@ struct Cfg {
     static constexpr int VSTAGES = 32768 / KV_STAGE;
     static constexpr int KV_DBLK = CHUNK * ROW_BYTES;  // one 64-column block of a stage
     static constexpr int Q_DBLK = BM * ROW_BYTES;
-    // [0, Q_BYTES): the Q tile as loaded; once the row threads have copied it into TMEM, the
-    // same bytes stage the block's output for its TMA store, and then take the Q tile of the
-    // CTA's block after next.
+    // [0, Q_BYTES): the Q tile as loaded; once it is copied into TMEM, the same bytes stage the
+    // previous block's output for its TMA store, and then take the Q tile of the next block.
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + Q_BYTES;
     static constexpr int V_OFF = K_OFF + KSTAGES * KV_STAGE;
@@ -104,14 +104,15 @@ struct Cfg {
     // waited for in order, so no parity wait has two of its phases outstanding.
     static constexpr int B_PV = B_PR + NB;
     static constexpr int B_OF = B_PV + NB;   // O of the block complete (after its last PV)
-    static constexpr int B_QT = B_OF + 1;    // Q of the block copied into TMEM (128 arrivals)
+    static constexpr int B_QT = B_OF + 1;    // Q of the block copied into TMEM (its shared buffer read)
     static constexpr int B_STF = B_QT + 1;   // output of the block staged (128 arrivals)
     static constexpr int B_STR = B_STF + 1;  // staged output read by its TMA store
     static constexpr int B_DR = B_STR + 1;   // drain of the S issuer's MMAs
     static constexpr int B_DR2 = B_DR + 1;   // drain of the PV issuer's MMAs
-    static constexpr int NBARS = B_DR2 + 1;
+    static constexpr int B_SD = B_DR2 + 1;   // S products of the block done (its Q no longer read)
+    static constexpr int NBARS = B_SD + 1;
     static constexpr bool counts128(int idx) {
-        return (idx >= B_PR && idx < B_PR + NB) || idx == B_QT || idx == B_STF;
+        return (idx >= B_PR && idx < B_PR + NB) || idx == B_STF;
     }
     static constexpr int BAR_BYTES = NBARS * 8 + 16;  // + TMEM address and abort flag
     static_assert(BAR_BYTES <= 512, "barriers must fit the alignment gap or its complement");
@@ -330,27 +331,6 @@ __device__ __forceinline__ void describe_block(int L, const TcArgs &a, BlockDesc
     }
 }
 
-// This row of a Q tile (staged in shared memory, 128B-swizzled) into TMEM lane (the calling
-// thread's), columns Q_COL + w holding the bf16 pair (q[2w], q[2w+1]): the A operand layout
-// of the S products.  One out-of-line copy: it runs once per block.
-template <int D>
-static __device__ __noinline__ void copy_q_row(const uint8_t *qrow, int swz, uint32_t taddr) {
-#pragma unroll 1
-    for (int dc = 0; dc < D / 64; ++dc) {
-        uint32_t wq[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {  // 8 bf16 of the row per 16-byte chunk
-            const uint4 u4 = *reinterpret_cast<const uint4 *>(qrow + dc * BM * ROW_BYTES + ((ch ^ swz) << 4));
-            wq[4 * ch] = u4.x;
-            wq[4 * ch + 1] = u4.y;
-            wq[4 * ch + 2] = u4.z;
-            wq[4 * ch + 3] = u4.w;
-        }
-        tmem_st16(taddr + dc * 32, wq);
-        tmem_st16(taddr + dc * 32 + 16, wq + 16);
-    }
-}
-
 // The fused gate's output for one row ("pi-Attention" page, 2.3: a light MLP per token and per
 // head): pre holds the row's hidden pre-activations W1_h q (the tensor core's product of the Q
 // tile with the W1 rows of the block's heads); returns alpha = 1 / (1 + exp(-z)) with
@@ -513,7 +493,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // next block's Q tile.  At V tile t_st of block k (t_st = min(4, tiles - 1)) the output
         // of block k-1 is staged (its PV products finished long ago), so it is stored from the
         // shared buffer, and once that store has read the buffer the Q tile of block k+1 takes
-        // its place (the row threads copied the Q tile of block k into TMEM before staging).
+        // its place (the Q tile of block k was copied into TMEM before the output was staged).
         if (lane == 0) {
             prefetch_tmap(&tmV);
             prefetch_tmap(&tmO);
@@ -588,10 +568,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int L = L0; ok && L < args.n_blocks; L = next_block(L), ++k) {
             BlockDesc bd;
             describe_block(L, args, bd);
-            // the Q tile of this block is in TMEM (copied once the previous block's S products
-            // were done)
-            ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_QT), (uint32_t)(k & 1), wc));
+            // The block's Q tile into TMEM, as the A operand of its S products: once the previous
+            // block's S products are done with the old one, and the tile has landed in shared
+            // memory, one copy per 16 elements of d; the S products below execute after them.
+            bool w = (k == 0) || wait_bar(bar(C::B_SD), (uint32_t)((k - 1) & 1), wc);
+            if (w) w = wait_bar(bar(C::B_Q), (uint32_t)(k & 1), wc);
+            ok = __all_sync(0xffffffffu, w);
             if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint64_t q0 = sdesc(sQ, 16, 1024);
+#pragma unroll
+                for (int dc = 0; dc < C::KD; ++dc)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tmem_cp_128x256b(aQ + (dc * 4 + ks) * 8, q0 + (uint64_t)((dc * C::Q_DBLK + ks * 32) >> 4));
+                tc_commit(bar(C::B_QT));  // the shared buffer is read once the copies are done
+            }
+            __syncwarp();
             if (k == 0 && lane == 0) stamp(3);
             for (int t = 0; t < bd.n_tiles + G0; ++t, ++gs) {
                 const int st = (int)(gs % KST), buf = (int)(gs % NB);
@@ -618,6 +612,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     tc_commit(bar(C::B_SF + buf));
                     tc_commit(bar(C::B_KE + st));
+                    if (t == bd.n_tiles + G0 - 1) tc_commit(bar(C::B_SD));
                 }
                 __syncwarp();
                 if (k == 0 && lane == 0) stamp_tile(40, t);
@@ -694,25 +689,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const float sc = s.scale_log2;
 
-        // This row of block bd's Q tile into TMEM (rows past N hold the TMA's zero fill).
-        // Returns the row's input alpha (the fused gate's comes from the block's gate tile),
-        // loaded after the out-of-line copy (a load in flight across a call would be waited for
-        // there); it was prefetched into L2 a block ahead.
-        auto copy_q = [&](const BlockDesc &bd, int kb, float &al_out) -> bool {
-            const int iq = bd.p0 - s.qoff + trow, h = bd.h0 + hh;
-            const bool row_ok = iq < s.nq;
-            const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
-            if (!__all_sync(0xffffffffu, wait_bar(bar(C::B_Q), (uint32_t)(kb & 1), wc))) return false;
-            copy_q_row<D>(smem + C::Q_OFF + r * ROW_BYTES, r & 7, tbase + lane_base + C::Q_COL);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_QT));
-            if (!GATE) al_out = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
-            return true;
+        // This row's input alpha in block L (1 where none is given or the row is past the
+        // window; the fused gate's comes from the block's gate tile).  Each block's alpha is
+        // prefetched into L2 two blocks ahead and loaded one block ahead.
+        const bool use_alpha = !GATE && args.alpha != nullptr;
+        auto alpha_ptr = [&](int L) -> const float * {
+            const int rest = args.div_nqb.div(L);
+            const int bn = args.div_ngrp.div(rest);
+            const int in = (L - rest * args.nqb) * R + trow;
+            if (!use_alpha || in >= s.nq) return nullptr;
+            return args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.nq + in;
         };
-
-        float al_next = 1.f;
-        bool ok = copy_q(bd0, 0, al_next);
+        const float *pa0 = alpha_ptr(L0);
+        float al_next = pa0 ? *pa0 : 1.f;
+        if (L0 < args.n_blocks - LS) {
+            const float *pa = alpha_ptr(L0 + LS);
+            if (pa) prefetch_l2(pa);
+        }
+        bool ok = true;
         uint32_t gsm = 0;
         int k = 0;
         for (int L = L0; ok && L < args.n_blocks; L = next_block(L), ++k) {
@@ -723,6 +717,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const bool row_ok = iq < s.nq;
             const long long row_g = ((long long)bd.b * s.H + h) * s.nq + iq;
             float al = al_next;  // the fused gate sets it at the block's first tile
+            if (has_next) {      // L + LS < n_blocks
+                const float *pa = alpha_ptr(L + LS);
+                al_next = pa ? *pa : 1.f;
+            }
+            if (L < args.n_blocks - 2 * LS) {
+                const float *pa = alpha_ptr(L + 2 * LS);
+                if (pa) prefetch_l2(pa);
+            }
             float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
             float off_skip = log2f(1.f - al);
             const int lo_i = band_lo(i, s.mode, s.k_local);
@@ -732,15 +734,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
             float m_ref = -INFINITY, l = 0.f;
             long long cnt = 0, isum = 0;
-            if (has_next && args.alpha) {  // the next block's alpha into L2, a block ahead
-                const int Ln = L + LS;     // < n_blocks
-                const int rest = args.div_nqb.div(Ln);
-                const int bn = args.div_ngrp.div(rest);
-                const int in = (Ln - rest * args.nqb) * R + trow;
-                if (in < s.nq)
-                    prefetch_l2(args.alpha + ((long long)bn * s.H + (rest - bn * args.ngrp) * args.GP + hh) * s.nq + in);
-            }
-
             for (int t = 0; t < bd.n_tiles + G0; ++t, ++gsm) {
                 const int buf = (int)(gsm % NB);
                 if (DBG == 3 && warp == 4 && lane == 0) ok = timed_wait(bar(C::B_SF + buf), (gsm / NB) & 1, 168, t);
@@ -878,22 +871,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (k == 0 && warp == 4 && lane == 0) stamp_tile(88, t);
             }
 
-            // The block's S products are done, so its Q tile in TMEM is no longer read: the next
-            // block's Q tile takes its place now, letting that block's first S products overlap
-            // this block's epilogue.
-            if (ok && has_next) {
-                BlockDesc nx;
-                describe_block(L + LS, args, nx);  // L + LS < n_blocks
-                ok = copy_q(nx, k + 1, al_next);
-            }
             // ---- epilogue: O / l -> bf16 -> shared (swizzled) -> TMA store by warp 2.  A parity
             // wait names a phase only if the barrier is at most one phase away from it; by now
             // the PV barrier may be anywhere from n_tiles-2 to n_tiles phases along, so the
-            // epilogue waits on the block's O barrier.  The staging buffer holds the next
-            // block's Q tile until this thread copied its row, and the previous block's output
-            // until warp 2's store has read it.
+            // epilogue waits on the block's O barrier.  The staging buffer holds the previous
+            // block's output until warp 2's store has read it, and then the next block's Q tile
+            // until the S issuer's copies into TMEM have read it.  (That copy's barrier is one
+            // phase on from this block's, which had completed before this block's S products:
+            // the copies execute ahead of them.)
             if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_OF), (uint32_t)(k & 1), wc));
             if (ok && k > 0) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_STR), (uint32_t)((k - 1) & 1), wc));
+            if (ok && has_next) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_QT), (uint32_t)((k + 1) & 1), wc));
             if (k == 0 && warp == 4 && lane == 0) stamp(4);
             if (!ok) break;
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
