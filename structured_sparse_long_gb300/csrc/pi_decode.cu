@@ -13,9 +13,14 @@
 //   * Thread 0 stages each chunk's K and V rows in shared memory with bulk copies
 //     (cp.async.bulk, one per contiguous band run and one per skip row) into a two-stage ring
 //     completed by an mbarrier.
-//   * Warp w handles the query heads w, w+4, ... of the GQA group.  Lanes split d for the dot
-//     products (conflict-free 256-byte row reads), a butterfly reduce-scatter leaves lane t
-//     with the score of key t, and the warp keeps an online softmax state per head.
+//   * Groups of at most 4 query heads (KSG > 0): warp w takes keys 8w .. 8w+7 of each chunk for
+//     every head of the group, so that each K and V row is unpacked once for all of them.
+//     Lanes split d for the dot products (conflict-free 256-byte row reads); one butterfly
+//     reduce-scatter of the 8 x KSG partial scores leaves lane t with key t & 7 of head
+//     (t & (8 KSG - 1)) >> 3; each lane keeps its head's online softmax state and every lane
+//     the output slice of every head.  The four warps' states are merged in the CTA first.
+//   * Larger groups: warp w handles the query heads w, w+4, ... for all 32 keys of a chunk,
+//     with one reduce-scatter per head (lane t: key t).
 //   * The P partial states (m, l, o) of head hh are merged by CTA hh % P of the cluster through
 //     distributed shared memory (vector loads, all issued before use), which writes out (bf16)
 //     and lse.
@@ -38,6 +43,7 @@ using tc::WaitCtx;
 constexpr int WARPS = 4;
 constexpr int THREADS = WARPS * 32;
 constexpr int KEYS = 32;     // keys per chunk: one lane per key
+constexpr int NST = 2;       // chunk stages in the shared-memory ring (3 or 4 ran 32 and 33 us at D4)
 constexpr int MAX_P = 8;     // CTAs per cluster (portable limit)
 constexpr int MAX_G = 16;    // query heads per KV head
 constexpr unsigned kFull = 0xffffffffu;
@@ -57,10 +63,10 @@ template <int D>
 struct Lay {
     static constexpr int ROW = D * 2;                       // bytes of one bf16 row
     static constexpr int STAGE = 2 * KEYS * ROW;            // K then V rows of one chunk
-    static constexpr int PART_OFF = 2 * STAGE;              // partial states after the ring
+    static constexpr int PART_OFF = NST * STAGE;            // partial states after the ring
     static constexpr int PART = (D + 4) * 4;                // o[D], m, l of one head (fp32), 16-B rows
-    static constexpr int BAR_OFF = PART_OFF + MAX_G * PART; // full[2], abort flag
-    static constexpr int BYTES = BAR_OFF + 32;
+    static constexpr int BAR_OFF = PART_OFF + MAX_G * PART; // full[NST], abort flag
+    static constexpr int BYTES = BAR_OFF + 8 * NST + 16;
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -112,15 +118,17 @@ __device__ __forceinline__ void lds_bf16(const uint8_t *p, float *f) {
     }
 }
 
-// HPW: query heads per warp, ceil(G / 4) rounded up to 1, 2 or 4 (registers scale with it).
-template <int D, int HPW>
+// KSG > 0: every warp takes all heads (KSG, a power of two, at least G) for 8 keys of each chunk.
+// KSG = 0: HPW query heads per warp, ceil(G / 4) rounded up to 1, 2 or 4, for all 32 keys.
+// (Registers scale with the heads a warp holds.)
+template <int D, int HPW, int KSG>
 __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     using L = Lay<D>;
     constexpr int E = D / 32;  // columns per lane
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sbase = tc::smem_u32(smem);
     const uint32_t bar0 = sbase + L::BAR_OFF;
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::BAR_OFF + 16);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::BAR_OFF + 8 * NST);
     float *part = reinterpret_cast<float *>(smem + L::PART_OFF);
 
     const Shape &s = a.s;
@@ -135,8 +143,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     const int n_local = (a.n_chunks > r) ? (a.n_chunks - r + P - 1) / P : 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar0, 1);
-        mbar_init(bar0 + 8, 1);
+        for (int x = 0; x < NST; ++x) mbar_init(bar0 + 8 * x, 1);
         *abort_flag = 0u;
         tc::fence_barrier_init();
     }
@@ -146,11 +153,11 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     auto key_row = [&](int t) -> int {
         return t < a.n_band ? a.lo + t : (s.N - 1) - (a.m_first + t - a.n_band) * s.period;
     };
-    // chunk c of this CTA (global chunk r + c*P) into ring stage c & 1 (thread 0 only)
+    // chunk c of this CTA (global chunk r + c*P) into ring stage c % NST (thread 0 only)
     int issued = 0;
     auto issue = [&](int c) {
         issued = c + 1;
-        const int qc = r + c * P, st = c & 1;
+        const int qc = r + c * P, st = c % NST;
         const int t0 = qc * KEYS, t1 = min(t0 + KEYS, a.n_keys);
         const uint32_t sk = sbase + st * L::STAGE, sv = sk + KEYS * L::ROW;
         const uint32_t bar = bar0 + 8 * st;
@@ -169,14 +176,15 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
         }
     };
     if (threadIdx.x == 0) {
-        for (int c = 0; c < min(2, n_local); ++c) issue(c);
+        for (int c = 0; c < min(NST, n_local); ++c) issue(c);
     }
 
     // ---- per-warp heads: query slice, prior, online state
-    float qv[HPW][E], o[HPW][E], m[HPW], l[HPW], offb[HPW], offs[HPW];
+    constexpr int NH = KSG > 0 ? KSG : HPW;  // heads whose query slice the warp holds
+    float qv[NH][E], o[NH][E], m[NH], l[NH], offb[NH], offs[NH];
 #pragma unroll
-    for (int j = 0; j < HPW; ++j) {
-        const int hh = warp + WARPS * j;
+    for (int j = 0; j < NH; ++j) {
+        const int hh = KSG > 0 ? j : warp + WARPS * j;
         m[j] = -INFINITY;
         l[j] = 0.f;
         offb[j] = 0.f;
@@ -198,14 +206,91 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
 
     bool ok = true;
     for (int c = 0; c < n_local; ++c) {
-        const int st = c & 1;
-        ok = wait_bar(bar0 + 8 * st, (c >> 1) & 1, wc);
+        const int st = c % NST;
+        ok = wait_bar(bar0 + 8 * st, (c / NST) & 1, wc);
         ok = __syncthreads_and(ok);
         if (!ok) break;
         const int t0 = (r + c * P) * KEYS;
         const int nk = min(KEYS, a.n_keys - t0);
-        const bool band_key = t0 + lane < a.n_band;
         const uint8_t *sk = smem + st * L::STAGE, *sv = sk + KEYS * L::ROW;
+        if constexpr (KSG > 0) {
+            // keys 8 warp + [0, 8) of the chunk, every head: V partial scores per lane
+            constexpr int V = 8 * KSG;
+            float pd[V];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int t = 8 * warp + kk;
+                float kf[E];
+                if (t < nk) {
+                    lds_bf16<E>(sk + t * L::ROW + lane * E * 2, kf);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) kf[e] = 0.f;
+                }
+#pragma unroll
+                for (int h = 0; h < KSG; ++h) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc = fmaf(qv[h][e], kf[e], acc);
+                    pd[h * 8 + kk] = acc;
+                }
+            }
+            // reduce-scatter over the low lane bits (value index h * 8 + kk = lane & (V - 1)),
+            // then the sum over the others
+#pragma unroll
+            for (int w = V / 2; w >= 1; w >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const float send = up ? pd[i] : pd[i + w];
+                    const float keep = up ? pd[i + w] : pd[i];
+                    pd[i] = keep + __shfl_xor_sync(kFull, send, w);
+                }
+            }
+#pragma unroll
+            for (int w = V; w < 32; w <<= 1) pd[0] += __shfl_xor_sync(kFull, pd[0], w);
+            // this lane: key kl of the warp's 8, head hl; the 8 lanes of a head share its state
+            const int hl = (lane & (V - 1)) >> 3, tk = 8 * warp + (lane & 7);
+            float ob = offb[0], os = offs[0];
+#pragma unroll
+            for (int h = 1; h < KSG; ++h)
+                if (hl == h) {
+                    ob = offb[h];
+                    os = offs[h];
+                }
+            const float z = (tk < nk && hl < G) ? pd[0] + ((t0 + tk < a.n_band) ? ob : os) : -INFINITY;
+            float mx = z;
+#pragma unroll
+            for (int w = 4; w; w >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, w));
+            const float mn = fmaxf(m[0], mx);
+            const float corr = (mn == -INFINITY) ? 1.f : exp2f(m[0] - mn);
+            const float p = (z == -INFINITY) ? 0.f : exp2f(z - mn);
+            float ps = p;
+#pragma unroll
+            for (int w = 4; w; w >>= 1) ps += __shfl_xor_sync(kFull, ps, w);
+            l[0] = l[0] * corr + ps;
+            m[0] = mn;
+#pragma unroll
+            for (int h = 0; h < KSG; ++h) {
+                const float ch = __shfl_sync(kFull, corr, h * 8);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[h][e] *= ch;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int t = 8 * warp + kk;
+                if (t >= nk) break;  // uniform per warp
+                float vf[E];
+                lds_bf16<E>(sv + t * L::ROW + lane * E * 2, vf);
+#pragma unroll
+                for (int h = 0; h < KSG; ++h) {
+                    const float ph = __shfl_sync(kFull, p, h * 8 + kk);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
+                }
+            }
+        } else {
+        const bool band_key = t0 + lane < a.n_band;
 #pragma unroll
         for (int j = 0; j < HPW; ++j) {
             if (warp + WARPS * j >= G) break;  // uniform per warp
@@ -256,27 +341,81 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
             }
             m[j] = mn;
         }
+        }
         __syncthreads();  // stage st is free again
-        if (threadIdx.x == 0 && c + 2 < n_local) issue(c + 2);
+        if (threadIdx.x == 0 && c + NST < n_local) issue(c + NST);
     }
-    if (!ok && threadIdx.x == 0) {  // let copies in flight (the last two issued) land first
+    if (!ok && threadIdx.x == 0) {  // let copies in flight (the last NST issued) land first
         volatile uint32_t zero = 0;
         WaitCtx w2{&zero, nullptr, 20000000ull};
-        for (int c = max(0, issued - 2); c < issued; ++c) wait_bar(bar0 + 8 * (c & 1), (c >> 1) & 1, w2);
+        for (int c = max(0, issued - NST); c < issued; ++c) wait_bar(bar0 + 8 * (c % NST), (c / NST) & 1, w2);
     }
 
-    // ---- partial states to shared memory, merged by CTA 0 of the cluster
+    // ---- partial states to shared memory (per head: o[D], m, l), merged across the cluster
+    if constexpr (KSG > 0) {
+        // the warps' states first, [warp][head] over the same space (4 x KSG <= 16 heads' room),
+        // then warp h merges head h's four into slot h, which only it reads
 #pragma unroll
-    for (int j = 0; j < HPW; ++j) {
-        const int hh = warp + WARPS * j;
-        if (hh >= G) break;
-        float *ps = part + hh * (D + 4);
-        if (lane == 0) {
-            ps[D] = ok ? m[j] : -INFINITY;
-            ps[D + 1] = ok ? l[j] : 0.f;
+        for (int h = 0; h < KSG; ++h) {
+            if (h >= G) break;
+            float *ps = part + (warp * KSG + h) * (D + 4);
+#pragma unroll
+            for (int e = 0; e < E; ++e) ps[lane * E + e] = ok ? o[h][e] : 0.f;
+            if (lane == h * 8) {  // a lane of head h
+                ps[D] = ok ? m[0] : -INFINITY;
+                ps[D + 1] = ok ? l[0] : 0.f;
+            }
         }
+        __syncthreads();
+        if (warp < G) {
+            const int h = warp;
+            float mw[WARPS], lw[WARPS], ow[WARPS][E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) ps[lane * E + e] = ok ? o[j][e] : 0.f;
+            for (int w = 0; w < WARPS; ++w) {
+                const float *ps = part + (w * KSG + h) * (D + 4);
+                mw[w] = ps[D];
+                lw[w] = ps[D + 1];
+#pragma unroll
+                for (int e = 0; e < E; ++e) ow[w][e] = ps[lane * E + e];
+            }
+            __syncwarp();
+            float mt = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w) mt = fmaxf(mt, mw[w]);
+            float lt = 0.f, ot[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) ot[e] = 0.f;
+            if (mt != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < WARPS; ++w) {
+                    if (mw[w] == -INFINITY) continue;
+                    const float f = exp2f(mw[w] - mt);
+                    lt = fmaf(f, lw[w], lt);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) ot[e] = fmaf(f, ow[w][e], ot[e]);
+                }
+            }
+            float *ps = part + h * (D + 4);
+#pragma unroll
+            for (int e = 0; e < E; ++e) ps[lane * E + e] = ot[e];
+            if (lane == 0) {
+                ps[D] = mt;
+                ps[D + 1] = lt;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+            const int hh = warp + WARPS * j;
+            if (hh >= G) break;
+            float *ps = part + hh * (D + 4);
+            if (lane == 0) {
+                ps[D] = ok ? m[j] : -INFINITY;
+                ps[D + 1] = ok ? l[j] : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) ps[lane * E + e] = ok ? o[j][e] : 0.f;
+        }
     }
     cluster_sync();
     // head hh is merged by CTA hh % P of the cluster, its warps taking those heads in turn; all
@@ -320,8 +459,17 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const DecArgs a) {
     cluster_sync();  // every CTA's shared memory stays alive until the others have read it
 }
 
-template <int D, int HPW>
+template <int D, int HPW, int KSG>
 static cudaError_t launch(const DecArgs &a, int P, cudaStream_t st) {
+    static PerDeviceOnce configured;  // shared memory above the 48 KB default
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured.needed(dev)) {
+        const cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HPW, KSG>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::BYTES);
+        if (e != cudaSuccess) return e;
+        configured.mark(dev);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P, (unsigned)a.s.Hkv, (unsigned)a.s.B);
     cfg.blockDim = dim3(THREADS, 1, 1);
@@ -334,7 +482,7 @@ static cudaError_t launch(const DecArgs &a, int P, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, HPW>, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, HPW, KSG>, a);
 }
 
 }  // namespace dec
@@ -379,16 +527,22 @@ cudaError_t launch_decode(const LaunchDecode &L, cudaStream_t st) {
     const long long pairs = (long long)s.B * s.Hkv;
     int P = (int)std::min<long long>(MAX_P, std::max<long long>(1, (2LL * sms + pairs - 1) / pairs));
     P = std::max(1, std::min(P, a.n_chunks));
+    // groups of up to 4 heads: key-split warps (KSG = G rounded up to a power of two); larger
+    // groups: ceil(G / 4) heads per warp
     const int hpw = (G + WARPS - 1) / WARPS;
     if (s.d == 64) {
-        if (hpw <= 1) return launch<64, 1>(a, P, st);
-        if (hpw <= 2) return launch<64, 2>(a, P, st);
-        return launch<64, 4>(a, P, st);
+        if (G <= 1) return launch<64, 1, 1>(a, P, st);
+        if (G <= 2) return launch<64, 2, 2>(a, P, st);
+        if (G <= 4) return launch<64, 4, 4>(a, P, st);
+        if (hpw <= 2) return launch<64, 2, 0>(a, P, st);
+        return launch<64, 4, 0>(a, P, st);
     }
     if (s.d == 128) {
-        if (hpw <= 1) return launch<128, 1>(a, P, st);
-        if (hpw <= 2) return launch<128, 2>(a, P, st);
-        return launch<128, 4>(a, P, st);
+        if (G <= 1) return launch<128, 1, 1>(a, P, st);
+        if (G <= 2) return launch<128, 2, 2>(a, P, st);
+        if (G <= 4) return launch<128, 4, 4>(a, P, st);
+        if (hpw <= 2) return launch<128, 2, 0>(a, P, st);
+        return launch<128, 4, 0>(a, P, st);
     }
     return cudaErrorInvalidValue;
 }
