@@ -398,11 +398,83 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 }
                 if (!live) { clo = CHUNK; chi = -1; }
                 const float bo = off - lse2;
+                const uint32_t tS = bcol + C::S_COL + cc * CHUNK, tP = bcol + C::DP_COL + cc * CHUNK;
+                const uint32_t oS = bcol + C::S_COL + cc * (CHUNK / 2), oP = bcol + C::DP_COL + cc * (CHUNK / 2);
+                if (!__any_sync(0xffffffffu, clo <= chi)) {
+                    // no row of the warp attends here (a skip chunk of other rows): zero operands
+                    const uint32_t zw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    tmem_st8(oS, zw);
+                    tmem_st8(oP, zw);
+                    tmem_st8(oS + 8, zw);
+                    tmem_st8(oP + 8, zw);
+                    continue;
+                }
+                if (sk) {
+                    // skip chunk: one column per row (its diagonal key), read with a select tree
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tS, sr);
+                    tmem_ld32(tP, dr);
+                    tmem_wait_ld();
+                    const bool v = clo <= chi;
+                    const int cs = v ? clo : 0;
+                    const float p = v ? fast_exp2(fmaf(select32(reinterpret_cast<const float *>(sr), cs), sc, bo)) : 0.f;
+                    const float w = p * select32(reinterpret_cast<const float *>(dr), cs);
+                    dsum += w;
+                    skip_p += p;
+                    skip_pdp += w;
+                    const float a1 = fmaf(-p, cen, w);
+                    const uint32_t w1 = (cs & 1) ? pack_bf16(0.f, a1) : pack_bf16(a1, 0.f);
+                    const uint32_t w2 = (cs & 1) ? pack_bf16(0.f, p) : pack_bf16(p, 0.f);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pw[8], pp[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            const bool hit = v && (half * 8 + x == (cs >> 1));
+                            pw[x] = hit ? w1 : 0u;
+                            pp[x] = hit ? w2 : 0u;
+                        }
+                        tmem_st8(oS + half * 8, pw);
+                        tmem_st8(oP + half * 8, pp);
+                    }
+                    continue;
+                }
+                if (__all_sync(0xffffffffu, clo == 0 && chi == CHUNK - 1)) {
+                    // band chunk inside every row's band: no masks, f32x2 arithmetic
+                    const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo), mc2 = pack2(-cen, -cen);
+                    uint64_t ds2 = pack2(0.f, 0.f);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t sr[16], dr[16];
+                        tmem_ld16(tS + half * 16, sr);
+                        tmem_ld16(tP + half * 16, dr);
+                        tmem_wait_ld();
+                        uint32_t pw[8], pp[8];
+#pragma unroll
+                        for (int c = 0; c < 16; c += 2) {
+                            float z0, z1, a0, a1;
+                            unpack2(fma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, bo2), z0, z1);
+                            const float p0 = fast_exp2(z0), p1 = fast_exp2(z1);
+                            const uint64_t p2 = pack2(p0, p1);
+                            const uint64_t w2 = mul2(p2, pack2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])));
+                            ds2 = add2(ds2, w2);
+                            unpack2(fma2(p2, mc2, w2), a0, a1);  // p (dp - c)
+                            pp[c / 2] = pack_bf16(p0, p1);
+                            pw[c / 2] = pack_bf16(a0, a1);
+                        }
+                        tmem_st8(oS + half * 8, pw);
+                        tmem_st8(oP + half * 8, pp);
+                    }
+                    float d0, d1;
+                    unpack2(ds2, d0, d1);
+                    dsum += d0 + d1;
+                    continue;
+                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t sr[16], dr[16];
-                    tmem_ld16(bcol + C::S_COL + cc * CHUNK + half * 16, sr);
-                    tmem_ld16(bcol + C::DP_COL + cc * CHUNK + half * 16, dr);
+                    tmem_ld16(tS + half * 16, sr);
+                    tmem_ld16(tP + half * 16, dr);
                     tmem_wait_ld();
                     uint32_t pw[8], pp[8];
 #pragma unroll
@@ -414,17 +486,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         const float w0 = p0v * __uint_as_float(dr[c]);
                         const float w1 = p1v * __uint_as_float(dr[c + 1]);
                         dsum += w0 + w1;
-                        if (sk) {
-                            skip_p += p0v + p1v;
-                            skip_pdp += w0 + w1;
-                        }
                         pp[c / 2] = pack_bf16(p0v, p1v);
                         pw[c / 2] = pack_bf16(fmaf(-p0v, cen, w0), fmaf(-p1v, cen, w1));
                     }
                     // A1 operand p (dp - c) over the S columns, A2 operand p over the dP columns;
                     // both chunk halves' values are already in registers
-                    tmem_st8(bcol + C::S_COL + cc * (CHUNK / 2) + half * 8, pw);
-                    tmem_st8(bcol + C::DP_COL + cc * (CHUNK / 2) + half * 8, pp);
+                    tmem_st8(oS + half * 8, pw);
+                    tmem_st8(oP + half * 8, pp);
                 }
             }
             tmem_wait_st();
@@ -833,6 +901,65 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
             if (!key_ok) { clo = QC; chi = -1; }
             const float *xb = xvec + st * 2 * QC;
+            const unsigned any = __ballot_sync(0xffffffffu, clo <= chi);
+            if (any == 0u || sk) {
+                // skip chunk (one column per key, its diagonal query) or nothing for this warp: the
+                // valid columns of a warp's keys are consecutive and lie in one 32-column block
+                const int qb = any ? (__shfl_sync(0xffffffffu, clo, __ffs(any) - 1) >> 5) : -1;
+                const bool v = clo <= chi;
+                const int cs = clo & 31;
+                uint32_t w1 = 0u, w2 = 0u;
+                if (qb >= 0) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(bcol + C::ST_COL + qb * 32, sr);
+                    tmem_ld32(bcol + C::DPT_COL + qb * 32, dr);
+                    tmem_wait_ld();
+                    const int cq = v ? clo : 0;
+                    const float p = v ? fast_exp2(fmaf(select32(reinterpret_cast<const float *>(sr), cs), sc, xb[cq])) : 0.f;
+                    const float z = p * (select32(reinterpret_cast<const float *>(dr), cs) - xb[QC + cq]);
+                    w1 = (cs & 1) ? pack_bf16(0.f, p) : pack_bf16(p, 0.f);
+                    w2 = (cs & 1) ? pack_bf16(0.f, z) : pack_bf16(z, 0.f);
+                }
+#pragma unroll
+                for (int q = 0; q < QC / 32; ++q) {
+                    uint32_t pp[16], pz[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const bool hit = v && q == qb && x == (cs >> 1);
+                        pp[x] = hit ? w1 : 0u;
+                        pz[x] = hit ? w2 : 0u;
+                    }
+                    tmem_st16(bcol + C::ST_COL + q * 16, pp);
+                    tmem_st16(bcol + C::DPT_COL + q * 16, pz);
+                }
+            } else if (__all_sync(0xffffffffu, clo == 0 && chi == QC - 1)) {
+                // band chunk inside the band of every key of the warp: no masks, f32x2 arithmetic
+                const uint64_t sc2 = pack2(sc, sc), neg2 = pack2(-1.f, -1.f);
+#pragma unroll
+                for (int q = 0; q < QC / 32; ++q) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(bcol + C::ST_COL + q * 32, sr);
+                    tmem_ld32(bcol + C::DPT_COL + q * 32, dr);
+                    tmem_wait_ld();
+                    uint32_t pp[16], pz[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const int c0 = q * 32 + c;
+                        const uint64_t bias2 = *reinterpret_cast<const uint64_t *>(xb + c0);
+                        const uint64_t dd2 = *reinterpret_cast<const uint64_t *>(xb + QC + c0);
+                        float z0, z1, y0, y1;
+                        unpack2(fma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, bias2), z0, z1);
+                        const float p0 = fast_exp2(z0), p1 = fast_exp2(z1);
+                        const uint64_t p2 = pack2(p0, p1);
+                        // dz = p (dp - D)
+                        unpack2(mul2(p2, fma2(dd2, neg2, pack2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])))), y0, y1);
+                        pp[c / 2] = pack_bf16(p0, p1);
+                        pz[c / 2] = pack_bf16(y0, y1);
+                    }
+                    tmem_st16(bcol + C::ST_COL + q * 16, pp);
+                    tmem_st16(bcol + C::DPT_COL + q * 16, pz);
+                }
+            } else {
 #pragma unroll
             for (int q = 0; q < QC / 32; ++q) {  // 32 columns of S^T and dP^T per TMEM round trip
                 uint32_t sr[32], dr[32];
@@ -855,6 +982,7 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 }
                 tmem_st16(bcol + C::ST_COL + q * 16, pp);
                 tmem_st16(bcol + C::DPT_COL + q * 16, pz);
+            }
             }
             tmem_wait_st();
             tc_fence_before();
