@@ -470,6 +470,11 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     dsum += d0 + d1;
                     continue;
                 }
+                // general path: the row's valid columns [clo, chi] as a bit mask; a masked logit
+                // becomes -inf, whose exp2 is 0
+                const uint32_t mbits = (clo <= chi) ? ((0xffffffffu >> (31 - chi)) & (0xffffffffu << clo)) : 0u;
+                const uint64_t sc2 = pack2(sc, sc), bo2 = pack2(bo, bo), mc2 = pack2(-cen, -cen);
+                uint64_t ds2 = pack2(0.f, 0.f);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t sr[16], dr[16];
@@ -480,20 +485,25 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
                     for (int c = 0; c < 16; c += 2) {
                         const int c0 = half * 16 + c;
-                        const bool v0 = c0 >= clo && c0 <= chi, v1 = c0 + 1 >= clo && c0 + 1 <= chi;
-                        const float p0v = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), sc, bo)) : 0.f;
-                        const float p1v = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, bo)) : 0.f;
-                        const float w0 = p0v * __uint_as_float(dr[c]);
-                        const float w1 = p1v * __uint_as_float(dr[c + 1]);
-                        dsum += w0 + w1;
-                        pp[c / 2] = pack_bf16(p0v, p1v);
-                        pw[c / 2] = pack_bf16(fmaf(-p0v, cen, w0), fmaf(-p1v, cen, w1));
+                        float z0, z1, a0, a1;
+                        unpack2(fma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, bo2), z0, z1);
+                        const float p0 = fast_exp2(((mbits >> c0) & 1u) ? z0 : -INFINITY);
+                        const float p1 = fast_exp2(((mbits >> (c0 + 1)) & 1u) ? z1 : -INFINITY);
+                        const uint64_t p2 = pack2(p0, p1);
+                        const uint64_t w2 = mul2(p2, pack2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])));
+                        ds2 = add2(ds2, w2);
+                        unpack2(fma2(p2, mc2, w2), a0, a1);  // p (dp - c)
+                        pp[c / 2] = pack_bf16(p0, p1);
+                        pw[c / 2] = pack_bf16(a0, a1);
                     }
                     // A1 operand p (dp - c) over the S columns, A2 operand p over the dP columns;
                     // both chunk halves' values are already in registers
                     tmem_st8(oS + half * 8, pw);
                     tmem_st8(oP + half * 8, pp);
                 }
+                float d0, d1;
+                unpack2(ds2, d0, d1);
+                dsum += d0 + d1;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -960,8 +970,13 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                     tmem_st16(bcol + C::DPT_COL + q * 16, pz);
                 }
             } else {
+            // general path: the key's valid columns [clo, chi] as a bit mask per 32-column block; a
+            // masked logit becomes -inf, whose exp2 is 0
+            const uint64_t sc2 = pack2(sc, sc), neg2 = pack2(-1.f, -1.f);
 #pragma unroll
             for (int q = 0; q < QC / 32; ++q) {  // 32 columns of S^T and dP^T per TMEM round trip
+                const int lo = max(clo - 32 * q, 0), hi = min(chi - 32 * q, 31);
+                const uint32_t mbits = (lo <= hi) ? ((0xffffffffu >> (31 - hi)) & (0xffffffffu << lo)) : 0u;
                 uint32_t sr[32], dr[32];
                 tmem_ld32(bcol + C::ST_COL + q * 32, sr);
                 tmem_ld32(bcol + C::DPT_COL + q * 32, dr);
@@ -970,15 +985,16 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     const int c0 = q * 32 + c;
-                    const float2 bias = *reinterpret_cast<const float2 *>(xb + c0);
-                    const float2 dd = *reinterpret_cast<const float2 *>(xb + QC + c0);
-                    const bool v0 = c0 >= clo && c0 <= chi, v1 = c0 + 1 >= clo && c0 + 1 <= chi;
-                    const float p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), sc, bias.x)) : 0.f;
-                    const float p1 = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, bias.y)) : 0.f;
-                    const float z0 = p0 * (__uint_as_float(dr[c]) - dd.x);
-                    const float z1 = p1 * (__uint_as_float(dr[c + 1]) - dd.y);
+                    const uint64_t bias2 = *reinterpret_cast<const uint64_t *>(xb + c0);
+                    const uint64_t dd2 = *reinterpret_cast<const uint64_t *>(xb + QC + c0);
+                    float z0, z1, y0, y1;
+                    unpack2(fma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, bias2), z0, z1);
+                    const float p0 = fast_exp2(((mbits >> c) & 1u) ? z0 : -INFINITY);
+                    const float p1 = fast_exp2(((mbits >> (c + 1)) & 1u) ? z1 : -INFINITY);
+                    const uint64_t p2 = pack2(p0, p1);
+                    unpack2(mul2(p2, fma2(dd2, neg2, pack2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])))), y0, y1);
                     pp[c / 2] = pack_bf16(p0, p1);
-                    pz[c / 2] = pack_bf16(z0, z1);
+                    pz[c / 2] = pack_bf16(y0, y1);
                 }
                 tmem_st16(bcol + C::ST_COL + q * 16, pp);
                 tmem_st16(bcol + C::DPT_COL + q * 16, pz);
