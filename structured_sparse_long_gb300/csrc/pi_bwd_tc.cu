@@ -777,7 +777,27 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             }
         }
     } else if (warp == 2) {
-        // ================= per-query vectors of each chunk: bias = prior - lse (log2 units), D
+        // ================= per-query vectors of each chunk: bias = prior - lse (log2 units), D.
+        // The loads of chunk ci + 1 are in flight while chunk ci's values are stored.
+        constexpr int QL = QC / 32;  // queries per lane
+        float nl[QL], na[QL], nd[QL];
+        bool nsk = false;
+        auto fetch = [&](int ci) {
+            int hh, i0, back;
+            kw.chunk(ci, hh, i0, back, nsk);
+            const long long rbase = ((long long)b * s.H + g * G + hh) * s.nq;
+#pragma unroll
+            for (int e = 0; e < QL; ++e) {
+                // skip chunks of the bidirectional mode may start before 0; positions outside the
+                // query window (a sequence shard's halo) have no query and take P = 0
+                const int iq = i0 + lane + 32 * e - s.qoff;  // row of the query window
+                const bool in = iq >= 0 && iq < s.nq;
+                nl[e] = in ? args.lse[rbase + iq] : -INFINITY;
+                na[e] = (in && args.alpha) ? args.alpha[rbase + iq] : 1.f;
+                nd[e] = in ? args.Dws[rbase + iq] : 0.f;
+            }
+        };
+        if (n_chunks > 0) fetch(0);
         bool ok = true;
         for (int ci = 0; ok && ci < n_chunks; ++ci) {
             const int st = ci % ST, round = ci / ST;
@@ -786,26 +806,22 @@ bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             }
-            int hh, i0, back;
-            bool sk;
-            kw.chunk(ci, hh, i0, back, sk);
-            const long long rbase = ((long long)b * s.H + g * G + hh) * s.nq;
+            float cl[QL], ca[QL], cd[QL];
+#pragma unroll
+            for (int e = 0; e < QL; ++e) {
+                cl[e] = nl[e];
+                ca[e] = na[e];
+                cd[e] = nd[e];
+            }
+            const bool sk = nsk;
+            if (ci + 1 < n_chunks) fetch(ci + 1);
             float *xb = xvec + st * 2 * QC;
 #pragma unroll
-            for (int e = 0; e < QC / 32; ++e) {
-                const int c = lane + 32 * e, iq = i0 + c - s.qoff;  // row of the query window
-                float bias = -INFINITY, dv = 0.f;
-                // skip chunks of the bidirectional mode may start before 0; positions outside the
-                // query window (a sequence shard's halo) have no query and take P = 0
-                if (iq >= 0 && iq < s.nq) {
-                    const float lse2 = args.lse[rbase + iq] * kLog2e;
-                    const float al = args.alpha ? args.alpha[rbase + iq] : 1.f;
-                    const float prior = (s.mode == kModeEcp) ? 0.f : (sk ? log2f(1.f - al) : log2f(al));
-                    if (lse2 != -INFINITY) bias = prior - lse2;
-                    dv = args.Dws[rbase + iq];
-                }
-                xb[c] = bias;
-                xb[QC + c] = dv;
+            for (int e = 0; e < QL; ++e) {
+                const float lse2 = cl[e] * kLog2e;
+                const float prior = (s.mode == kModeEcp) ? 0.f : (sk ? log2f(1.f - ca[e]) : log2f(ca[e]));
+                xb[lane + 32 * e] = (lse2 != -INFINITY) ? prior - lse2 : -INFINITY;
+                xb[QC + lane + 32 * e] = cd[e];
             }
             mbar_arrive(bar(C::B_XF + st));
         }
