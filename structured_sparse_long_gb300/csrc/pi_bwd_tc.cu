@@ -339,6 +339,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int h = h0 + hh;
         const bool row_ok = i - s.qoff < s.nq;
         const long long row_g = ((long long)b * s.H + h) * s.nq + (i - s.qoff);
+        // the row's out (for the centre below) is loaded in the same round trip as its alpha
+        // and lse; its dout is the staged dO tile's row
+        uint4 orow_v[D / 8];
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+            orow_v[c] = row_ok ? __ldg(reinterpret_cast<const uint4 *>(args.out + row_g * D) + c) : make_uint4(0u, 0u, 0u, 0u);
         const float al = (args.alpha && row_ok) ? args.alpha[row_g] : 1.f;
         const float off_band = (s.mode != kModeEcp) ? log2f(al) : 0.f;
         const float off_skip = log2f(1.f - al);
@@ -352,22 +358,28 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         bool any_skip = false;
         bool ok = true;
         // centre c_i = dout_i . out_i (bf16 rows); D_i itself is accumulated exactly below
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_QF), 0, wc));  // the dO tile has landed
         float cen = 0.f;
         if (live) {
-            const __nv_bfloat16 *orow = args.out + row_g * D, *grow = args.dout + row_g * D;
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-            for (int c = 0; c < D; c += 8) {
-                float o8[8], g8[8];
-                load8(orow + c, o8);
-                load8(grow + c, g8);
+            const uint8_t *grow = smem + C::G_OFF + r * ROW_BYTES;
+            uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    acc0 = fmaf(o8[e], g8[e], acc0);
-                    acc1 = fmaf(o8[e + 1], g8[e + 1], acc1);
-                }
+            for (int c = 0; c < D / 8; ++c) {  // 8 elements per 16-byte chunk
+                const uint4 gv = *reinterpret_cast<const uint4 *>(grow + (c >> 3) * C::Q_DBLK + (((c & 7) ^ (r & 7)) << 4));
+                const uint4 ov = orow_v[c];
+                acc0 = fma2(pack2(__uint_as_float(ov.x << 16), __uint_as_float(ov.x & 0xffff0000u)),
+                            pack2(__uint_as_float(gv.x << 16), __uint_as_float(gv.x & 0xffff0000u)), acc0);
+                acc1 = fma2(pack2(__uint_as_float(ov.y << 16), __uint_as_float(ov.y & 0xffff0000u)),
+                            pack2(__uint_as_float(gv.y << 16), __uint_as_float(gv.y & 0xffff0000u)), acc1);
+                acc0 = fma2(pack2(__uint_as_float(ov.z << 16), __uint_as_float(ov.z & 0xffff0000u)),
+                            pack2(__uint_as_float(gv.z << 16), __uint_as_float(gv.z & 0xffff0000u)), acc0);
+                acc1 = fma2(pack2(__uint_as_float(ov.w << 16), __uint_as_float(ov.w & 0xffff0000u)),
+                            pack2(__uint_as_float(gv.w << 16), __uint_as_float(gv.w & 0xffff0000u)), acc1);
             }
-            cen = acc0 + acc1;
+            float x0, x1, y0, y1;
+            unpack2(acc0, x0, x1);
+            unpack2(acc1, y0, y1);
+            cen = (x0 + x1) + (y0 + y1);
         }
 
         for (int t = 0; t < n_tiles; ++t) {
