@@ -398,6 +398,12 @@ def setup_workload(w, pa, dev, stream):
     kernels it launches)."""
     inp = make_inputs(w, with_dout=w.backward)
     d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
+    return (inp,) + device_set(w, pa, dev, d, stream)
+
+
+def device_set(w, pa, dev, d, stream):
+    """Outputs, gradient buffers and the step's launchers for the device inputs d on `stream`:
+    returns (d, out, lse, gradient buffers, phases)."""
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.B, w.H) if w.decode else (w.B, w.H, w.N), device=dev, dtype=torch.float32)
     bufs = {}
@@ -434,7 +440,7 @@ def setup_workload(w, pa, dev, stream):
     else:
         # the backward is two kernels (query-major dq pass, key-major dk/dv pass) on either path
         phases = [("pi_attn_fwd", fwd, 1)] + ([("pi_attn_bwd", bwd, 2)] if w.backward else [])
-    return inp, d, out, lse, bufs, phases
+    return d, out, lse, bufs, phases
 
 
 def time_steps(w, pa, dev, stream, phases, steps, warmup, sampler=None, world=1):
@@ -548,7 +554,11 @@ def gpu_arm(args, w, rank, world, local_rank):
     # dominant kernel roofline (forward kernel: the whole step for the forward workloads)
     roofline = roofline_of(w, wk, per_phase)
 
-    # end to end through the public API with pinned host buffers
+    # End to end through the public API with pinned host buffers, as a stream of steps: every
+    # step copies its inputs to the device, runs, and copies its outputs back; two device buffer
+    # sets let step s+1's inputs travel (host to device) while step s runs and its outputs travel
+    # back (device to host), on three streams ordered by events.  (One copy stream per direction
+    # measured fastest: splitting the copies over 2, 4 or 8 streams ran 3-9 % slower at C4.)
     e2e = None
     if not args.no_e2e:
         if w.decode:  # per step: the new queries and gates, and the new token's K/V rows
@@ -568,36 +578,62 @@ def gpu_arm(args, w, rank, world, local_rank):
             grads_h = {n: torch.empty(bufs[n].shape, dtype=bufs[n].dtype).pin_memory()
                        for n in ("dq", "dk", "dv", "dalpha")}
             d2h += sum(t.numel() * t.element_size() for t in grads_h.values())
+        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        d2 = {n: (t.clone() if t is not None else None) for n, t in d.items()}
+        sets = [(d, out, lse, bufs, phases), device_set(w, pa, dev, d2, stream)]
+        torch.cuda.synchronize(dev)
+        ev_in = [torch.cuda.Event() for _ in sets]    # the set's inputs landed
+        ev_run = [torch.cuda.Event() for _ in sets]   # its step ran (inputs read, outputs written)
+        ev_back = [torch.cuda.Event() for _ in sets]  # its outputs copied back
 
-        def e2e_step():
-            for n, t in host.items():
-                if t is None or (n == "dout" and not w.backward):
-                    continue
-                if n in ("k_new", "v_new"):  # append the new token to the cache (row N-1)
-                    d[n[0]][:, :, w.N - 1].copy_(t, non_blocking=True)
-                else:
-                    d[n].copy_(t, non_blocking=True)
-            step()
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
-            for n, t in grads_h.items():
-                t.copy_(bufs[n], non_blocking=True)
+        def e2e_step(k):
+            b = k % 2
+            dd, o, ls, bf, ph = sets[b]
+            if k >= 2:
+                s_h2d.wait_event(ev_run[b])
+            with torch.cuda.stream(s_h2d):
+                for n, t in host.items():
+                    if t is None or (n == "dout" and not w.backward):
+                        continue
+                    if n in ("k_new", "v_new"):  # append the new token to the cache (row N-1)
+                        dd[n[0]][:, :, w.N - 1].copy_(t, non_blocking=True)
+                    else:
+                        dd[n].copy_(t, non_blocking=True)
+            ev_in[b].record(s_h2d)
+            stream.wait_event(ev_in[b])
+            if k >= 2:
+                stream.wait_event(ev_back[b])
+            for _, fn, _ in ph:
+                fn()
+            ev_run[b].record(stream)
+            s_d2h.wait_event(ev_run[b])
+            with torch.cuda.stream(s_d2h):
+                out_h.copy_(o, non_blocking=True)
+                lse_h.copy_(ls, non_blocking=True)
+                for n, t in grads_h.items():
+                    t.copy_(bf[n], non_blocking=True)
+            ev_back[b].record(s_d2h)
 
-        for _ in range(max(1, min(args.warmup, 3))):
-            e2e_step()
+        for k in range(max(2, min(args.warmup, 3))):
+            e2e_step(k)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, 10))
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        n_e2e = max(2, min(args.steps, 10))
+        e0.record(s_h2d)
+        for k in range(n_e2e):
+            e2e_step(k)
+        e1.record(s_d2h)  # after the last step's copy back (the stream is in order)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1)
         e_ms = reduce_max(e_ms, world, dev if args.backend == "nccl" else "cpu")
         e2e = {"value": tokens_per_step * n_e2e / (e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / n_e2e, "steps": n_e2e}
+               "ms_per_step": e_ms / n_e2e, "steps": n_e2e,
+               "pipelining": "two device buffer sets; host-to-device copies, the step and the "
+                             "device-to-host copies on three streams, so step s+1's inputs travel "
+                             "while step s runs"}
+        del sets, d2
+        torch.cuda.empty_cache()
 
     if rank != 0:
         return
