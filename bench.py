@@ -495,14 +495,42 @@ def time_steps(w, pa, dev, stream, phases, steps, warmup, sampler=None, world=1)
     return {n: [e[n][0].elapsed_time(e[n][1]) for e in ev] for n, _, _ in phases}
 
 
-def config_numbers(w, per_phase, steps):
+def time_l2_warm(pa, dev, stream, phases, steps=50, warmup=3):
+    """Mean ms per step of `steps` steps run back to back with no flush between them (the L2-warm
+    figure of a workload small enough to stay in L2), from one event pair around them all."""
+    def step():
+        for _, fn, _ in phases:
+            fn()
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if pa.status() != 0:
+        raise RuntimeError("device status word set during the L2-warm steps")
+    return e0.elapsed_time(e1) / steps
+
+
+def step_times(per_phase, steps):
+    """Per-step times (ms): the sum over the phases of each step."""
+    return [sum(v[k] for v in per_phase.values()) for k in range(steps)]
+
+
+def config_numbers(w, per_phase, steps, l2_warm_ms=None):
     """The metric's numbers for one workload from its per-phase times."""
     wk = work(w, w.backward)
     total_ms = sum(sum(v) for v in per_phase.values())
     tokens = w.B if w.decode else w.B * w.N
     roof = roofline_of(w, wk, per_phase)
+    extra = {"l2_warm_ms_per_step": l2_warm_ms} if l2_warm_ms is not None else {}
     return {"workload": f"{w.name}: {w.description}", "dtype": w.dtype,
-            "ms_per_step": total_ms / steps, "tokens_per_s": tokens * steps / (total_ms / 1e3),
+            "ms_per_step": total_ms / steps, **extra,
+            "median_ms_per_step": statistics.median(step_times(per_phase, steps)),
+            "tokens_per_s": tokens * steps / (total_ms / 1e3),
             "useful_tflops": wk["flops"] * steps / (total_ms / 1e3) / 1e12,
             "per_phase_ms": {n: statistics.mean(v) for n, v in per_phase.items()},
             "roofline": {k: roof[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
@@ -518,7 +546,9 @@ def other_configs(args, pa, dev, stream, names):
         w = WORKLOADS[name]
         phases = setup_workload(w, pa, dev, stream)[5]
         per_phase = time_steps(w, pa, dev, stream, phases, args.per_config_steps, 5)
-        res[name] = config_numbers(w, per_phase, args.per_config_steps)
+        warm = (time_l2_warm(pa, dev, stream, phases, args.per_config_steps)
+                if work(w, w.backward)["bytes"] < 2 * L2_BYTES else None)
+        res[name] = config_numbers(w, per_phase, args.per_config_steps, warm)
         del phases
         torch.cuda.empty_cache()
     return res
@@ -552,6 +582,8 @@ def gpu_arm(args, w, rank, world, local_rank):
     per_phase = time_steps(w, pa, dev, stream, phases, args.steps, args.warmup, sampler=sampler,
                            world=world)
     clocks = sampler.stop() if sampler else None
+    l2_warm = (time_l2_warm(pa, dev, stream, phases, min(args.steps, 200))
+               if rank == 0 and wk["bytes"] < 2 * L2_BYTES else None)
     step_ms = [sum(per_phase[n][k] for n, _, _ in phases) for k in range(args.steps)]
     total_ms = sum(step_ms)
     total_ms = reduce_max(total_ms, world, dev if args.backend == "nccl" else "cpu")
@@ -656,6 +688,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "median_ms_per_step": statistics.median(step_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded torch.Generator, shapes of the workload)",
             "config": config_block(w, l2_note), "useful_tflops": tflops,
@@ -663,6 +696,8 @@ def gpu_arm(args, w, rank, world, local_rank):
             "gpu_launches": args.steps * sum(n for _, _, n in phases),
             "clocks": clocks, "per_phase_ms": {n: statistics.mean(v) for n, v in per_phase.items()},
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if l2_warm is not None:  # the same steps back to back, L2 not flushed (rank 0's own)
+        line["l2_warm_ms_per_step"] = l2_warm
     if per_config is not None:
         line["per_config"] = per_config
     print(json.dumps(line), flush=True)
