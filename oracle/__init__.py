@@ -26,8 +26,11 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# PI_ORACLE_SRC builds the library from another copy of the C source (into its own directory):
+# tests/test_oracle_mutants.py plants one slip in such a copy and checks that the pins fail.
+_SRC = os.environ.get("PI_ORACLE_SRC") or os.path.join(_HERE, "oracle.c")
+_LIB = (os.path.join(os.path.dirname(os.path.abspath(_SRC)), "liboracle_alt.so")
+        if os.environ.get("PI_ORACLE_SRC") else os.path.join(_HERE, "liboracle.so"))
 _lock = threading.Lock()
 _lib = None
 
