@@ -888,18 +888,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_after();
             __syncwarp();
 #pragma unroll 1
-            for (int oh = 0; oh < D / 32; ++oh) {  // 32 fp32 columns per TMEM round trip
-                uint32_t x[32];
+            for (int oh = 0; oh < D / 32; oh += 2) {  // 64 fp32 columns per TMEM round trip
+                uint32_t x[64];
                 tmem_ld32(tbase + lane_base + C::O_COL + oh * 32, x);
+                tmem_ld32(tbase + lane_base + C::O_COL + oh * 32 + 32, x + 32);
                 tmem_wait_ld();
                 uint8_t *rowp = smem + C::Q_OFF + (oh >> 1) * C::Q_DBLK + r * ROW_BYTES;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {  // 8 columns -> one 16-byte chunk of the row
-                    const int cidx = (oh & 1) * 4 + w;
+                for (int w = 0; w < 8; ++w) {  // 8 columns -> one 16-byte chunk of the row
                     const float *f = reinterpret_cast<const float *>(x) + 8 * w;
                     const uint4 val = make_uint4(pack_bf16(f[0] * inv_l, f[1] * inv_l), pack_bf16(f[2] * inv_l, f[3] * inv_l),
                                                  pack_bf16(f[4] * inv_l, f[5] * inv_l), pack_bf16(f[6] * inv_l, f[7] * inv_l));
-                    *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (r & 7)) << 4)) = val;
+                    *reinterpret_cast<uint4 *>(rowp + ((w ^ (r & 7)) << 4)) = val;
                 }
             }
             // O is read: the next block's first PV may overwrite it once this thread marks that
