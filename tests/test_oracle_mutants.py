@@ -43,6 +43,17 @@ MUTANTS = [
     ("gate ReLU dropped", "if (pre > 0.0) z += w2[h * F + f] * pre;", "z += w2[h * F + f] * pre;"),
     ("gate hidden bias dropped", "double pre = b1[h * F + f];", "double pre = 0.0;"),
     ("gate logit doubled", "alpha[row] = 1.0 / (1.0 + exp(-z));", "alpha[row] = 1.0 / (1.0 + exp(-2.0 * z));"),
+    ("GQA group sum of dK/dV cut to one head",
+     "for (long h = g * G; h < (g + 1) * G; ++h) {", "for (long h = g * G; h < g * G + 1; ++h) {"),
+    ("scale dropped in dQ", "dqrow[c] += dz * kg[koff + c] * scale;", "dqrow[c] += dz * kg[koff + c];"),
+    ("gate output weights of head 0", "if (pre > 0.0) z += w2[h * F + f] * pre;", "if (pre > 0.0) z += w2[f] * pre;"),
+    ("gate output bias of head 0", "double z = b2[h];", "double z = b2[0];"),
+    ("ECP first segment's window clamped wrongly",
+     "        lo = (s - 1) * k_local;\n        if (lo < 0) lo = 0;",
+     "        lo = (s - 1) * k_local;\n        if (lo < 0) lo = k_local;"),
+    ("bidirectional band one key short on the right", "hi = i + k_local;", "hi = i + k_local - 1;"),
+    ("first skip multiple dropped",
+     "for (int m = 1; m <= S; ++m) {\n            long back", "for (int m = 2; m <= S; ++m) {\n            long back"),
 ]
 
 
